@@ -1,0 +1,188 @@
+"""CPU oracle for the batch-invariant GEMM y = x·W — TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may
+import this package.  The product (``invariant_bi_gemm_gb300``) never does, and the
+two share no code: the oracle is plain C (``bi_oracle.c``) built with gcc.
+
+Definition followed ("Batch-invariant matrix multiplication", nondeterminism
+article; the row-wise definition y[i] = f(x[i], W) of the batch-invariance issue,
+"Problem statement"):
+
+    y[i, j] = round_out( sum_{k ascending} dec(x[i, k]) * dec(w[k, j]) )   (fp64 sum)
+
+with a single round-to-nearest-even to the output dtype, and the absolute sum
+S_abs[i, j] = sum_k |dec(x[i, k]) * dec(w[k, j])| returned for the tolerance.
+
+Every function here is pinned by ``tests/test_oracle_*.py`` against exact
+rational arithmetic, the pages' worked examples and identities, and library
+routines; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+OUT_BF16 = 0
+OUT_F32 = 1
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        L.bio_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        L.bio_bf16_to_f64.restype = ctypes.c_double
+        L.bio_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.bio_e4m3_to_f64.restype = ctypes.c_double
+        L.bio_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+        L.bio_e8m0_to_f64.restype = ctypes.c_double
+        L.bio_f64_to_bf16.argtypes = [ctypes.c_double]
+        L.bio_f64_to_bf16.restype = ctypes.c_uint16
+        L.bio_f64_to_f32.argtypes = [ctypes.c_double]
+        L.bio_f64_to_f32.restype = ctypes.c_uint32
+        L.bio_gemm_f64.argtypes = [P, I64, I64, P, I64, P, P]
+        L.bio_gemm_f64.restype = ctypes.c_int
+        L.bio_gemm_bf16.argtypes = [P, I64, I64, P, I64, P, I64, ctypes.c_int, P, P, P]
+        L.bio_gemm_bf16.restype = ctypes.c_int
+        L.bio_gemm_mxfp8.argtypes = [P, P, I64, I64, P, P, I64, P, I64, P, P, P]
+        L.bio_gemm_mxfp8.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _rows_arg(rows, M):
+    if rows is None:
+        return None, M
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    return r, int(r.shape[0])
+
+
+def gemm_f64(x: np.ndarray, w: np.ndarray):
+    """fp64 inputs; returns (acc, sabs) fp64 [M, N] without output rounding."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    M, K = x.shape
+    K2, N = w.shape
+    assert K == K2
+    acc = np.empty((M, N), np.float64)
+    sabs = np.empty((M, N), np.float64)
+    rc = lib().bio_gemm_f64(_ptr(x), M, K, _ptr(w), N, _ptr(acc), _ptr(sabs))
+    if rc:
+        raise ValueError("bio_gemm_f64 rejected its arguments")
+    return acc, sabs
+
+
+def gemm_bf16(x: np.ndarray, w: np.ndarray, out: str = "bf16", rows=None):
+    """x uint16[M,K], w uint16[K,N] (bf16 patterns).
+
+    Returns (y, acc, sabs): y uint16 bf16 patterns or float32 values [R, N] where R is
+    len(rows) (the listed rows of x, in that order) or M; acc and sabs fp64 [R, N].
+    """
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    M, K = x.shape
+    K2, N = w.shape
+    assert K == K2
+    r, R = _rows_arg(rows, M)
+    if out == "bf16":
+        y = np.empty((R, N), np.uint16)
+        kind = OUT_BF16
+    elif out == "f32":
+        y = np.empty((R, N), np.uint32)
+        kind = OUT_F32
+    else:
+        raise ValueError(out)
+    acc = np.empty((R, N), np.float64)
+    sabs = np.empty((R, N), np.float64)
+    rc = lib().bio_gemm_bf16(_ptr(x), M, K, _ptr(w), N, _ptr(r), R, kind, _ptr(y), _ptr(acc), _ptr(sabs))
+    if rc:
+        raise ValueError("bio_gemm_bf16 rejected its arguments")
+    if out == "f32":
+        y = y.view(np.float32)
+    return y, acc, sabs
+
+
+def gemm_mxfp8(x, sx, w, sw, rows=None):
+    """x uint8[M,K] E4M3, sx uint8[M,K/32] E8M0, w uint8[K,N] E4M3, sw uint8[K/32,N] E8M0.
+
+    Returns (y bf16 patterns uint16 [R, N], acc, sabs) as gemm_bf16.
+    """
+    x = np.ascontiguousarray(x, dtype=np.uint8)
+    sx = np.ascontiguousarray(sx, dtype=np.uint8)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    sw = np.ascontiguousarray(sw, dtype=np.uint8)
+    M, K = x.shape
+    K2, N = w.shape
+    assert K == K2 and sx.shape == (M, K // 32) and sw.shape == (K // 32, N)
+    r, R = _rows_arg(rows, M)
+    y = np.empty((R, N), np.uint16)
+    acc = np.empty((R, N), np.float64)
+    sabs = np.empty((R, N), np.float64)
+    rc = lib().bio_gemm_mxfp8(_ptr(x), _ptr(sx), M, K, _ptr(w), _ptr(sw), N, _ptr(r), R,
+                              _ptr(y), _ptr(acc), _ptr(sabs))
+    if rc:
+        raise ValueError("bio_gemm_mxfp8 rejected its arguments")
+    return y, acc, sabs
+
+
+def bf16_to_f64(b) -> float:
+    return lib().bio_bf16_to_f64(int(b))
+
+
+def e4m3_to_f64(c) -> float:
+    return lib().bio_e4m3_to_f64(int(c))
+
+
+def e8m0_to_f64(e) -> float:
+    return lib().bio_e8m0_to_f64(int(e))
+
+
+def f64_to_bf16(v: float) -> int:
+    return int(lib().bio_f64_to_bf16(float(v)))
+
+
+def f64_to_f32_bits(v: float) -> int:
+    return int(lib().bio_f64_to_f32(float(v)))
+
+
+def bf16_array_to_f64(b: np.ndarray) -> np.ndarray:
+    """Vector decode through the oracle's own scalar decoder semantics (bits << 16)."""
+    b = np.asarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+# Tolerances from the unit roundoffs u(bf16) = 2^-8 and u(fp32) = 2^-24 of the
+# nondeterminism article ("Quantifying with unit roundoff"), as fixed for this GEMM:
+# bf16 output |y - y_ref| <= 4 * 2^-8 * S_abs, fp32 output |y - y_ref| <= 1e-5 * S_abs.
+TOL_BF16 = 4.0 * 2.0**-8
+TOL_F32 = 1e-5
+
+
+def tolerance_violations(y_gpu_f64: np.ndarray, y_ref_f64: np.ndarray, sabs: np.ndarray, tol: float):
+    """Return (count, max ratio |y - y_ref| / S_abs) under the rule |y - y_ref| <= tol * S_abs."""
+    d = np.abs(y_gpu_f64 - y_ref_f64)
+    bad = ~(d <= tol * sabs)   # NaN counts as a violation
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(sabs > 0, d / sabs, np.where(d == 0, 0.0, np.inf))
+    return int(bad.sum()), float(np.nanmax(ratio)) if ratio.size else 0.0
+
+
+__all__ = [
+    "gemm_f64", "gemm_bf16", "gemm_mxfp8", "bf16_to_f64", "e4m3_to_f64", "e8m0_to_f64",
+    "f64_to_bf16", "f64_to_f32_bits", "bf16_array_to_f64", "TOL_BF16", "TOL_F32",
+    "tolerance_violations", "lib",
+]
