@@ -1,0 +1,145 @@
+/*
+ * bi_gemm.h — C ABI of the batch-invariant GEMM library (libbi_gemm.so), sm_103a (GB300).
+ *
+ *     y[M, N] = x[M, K] · W[K, N]        fp32 accumulation
+ *
+ * Batch invariance is the row-wise definition y[i] = f(x[i], W) of the batch-invariance
+ * test issue (gitcode.com/CANN/ops-transformer/issues/2956, "Problem statement"): output
+ * row i depends only on input row i and the shared W, bit for bit, for every M and every
+ * content of the other rows.  The library gets it the way the nondeterminism article
+ * prescribes ("Batch-invariant matrix multiplication": compile one kernel configuration
+ * and use it for every shape): the tile shape, tcgen05 instruction shape, K order and
+ * split count are chosen once at bi_gemm_create from (K, N, dtype, scale_layout, SM
+ * count) and never from M.  Where a split count S > 1 is chosen, split s always covers
+ * the same K range and the S partials are merged in one fixed serial order ("[BI][DSv4]
+ * Make mHC tilelang ops batch invariant", "What": a pinned split count with a serial
+ * merge pins the reduction tree).  Results are also identical from run to run (no
+ * floating-point atomics; nondeterminism article, "Three kinds of determinism").
+ * Bit equality with other GPUs, drivers or library versions is not claimed.
+ *
+ * Conventions shared by all entry points:
+ *   - Return value: BI_GEMM_OK (0) or a negative BI_GEMM_ERR_* code; no entry point aborts
+ *     the process or prints.  bi_gemm_strerror() names a code.
+ *   - Layouts: row-major.  x is [M, K] (K contiguous), W is [K, N] (N contiguous), y is
+ *     [M, N] (N contiguous); no strides or transposes.
+ *   - Data pointers are DEVICE pointers owned by the caller, on the device that was
+ *     current at bi_gemm_create; they must stay valid until the work queued on `stream`
+ *     has finished.  `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - A handle is not thread-safe and must not be used on two streams at once.
+ *   - There is no fallback: a shape or layout the fixed configuration cannot serve is
+ *     refused at bi_gemm_create (fail closed), never routed to another kernel.
+ */
+#ifndef BI_GEMM_H
+#define BI_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct bi_gemm* bi_gemm_t;
+
+/* Input and output element types. */
+typedef enum {
+  BI_BF16_OUT_BF16 = 0,       /* x, W bf16; y bf16 (round to nearest even from fp32)     */
+  BI_BF16_OUT_F32 = 1,        /* x, W bf16; y fp32                                        */
+  BI_MXFP8E4M3_OUT_BF16 = 2   /* x, W OCP E4M3FN with E8M0 block scales; y bf16          */
+} bi_gemm_dtype;
+
+/* Scale layout.  BI_SCALES_E8M0_K32 (MXFP8 only): one E8M0 exponent per 32 consecutive K
+ * elements — sx[M, K/32] for the rows of x and sw[K/32, N] for the columns of W, both
+ * row-major uint8 (value 2^(e-127)); block kb covers k in [32*kb, 32*kb + 32).  This is the
+ * block-scaled MXFP8 format whose K-axis-varying scales are the known batch-invariance
+ * trigger of the batch-invariance test issue ("Test methodology"). */
+typedef enum {
+  BI_SCALES_NONE = 0,
+  BI_SCALES_E8M0_K32 = 1
+} bi_gemm_scale_layout;
+
+/* Device pointers to the two scale matrices (MXFP8 only). */
+typedef struct {
+  const uint8_t* sx; /* [M, K/32] E8M0, 4-byte aligned */
+  const uint8_t* sw; /* [K/32, N] E8M0                 */
+} bi_gemm_scales;
+
+enum {
+  BI_GEMM_OK = 0,
+  BI_GEMM_ERR_INVALID_ARG = -1,  /* null handle / pointer, negative size, bad enum        */
+  BI_GEMM_ERR_UNSUPPORTED = -2,  /* shape or dtype the fixed configuration cannot serve    */
+  BI_GEMM_ERR_ALIGNMENT = -3,    /* a pointer or row pitch breaks the 16-byte rule          */
+  BI_GEMM_ERR_CUDA = -4,         /* a CUDA runtime call failed (launch, allocation setup)   */
+  BI_GEMM_ERR_OOM = -5,          /* workspace allocation failed                             */
+  BI_GEMM_ERR_TIMEOUT = -6       /* a bounded in-kernel wait expired (reported by
+                                    bi_gemm_get_device_error)                               */
+};
+
+/* Create a handle for y = x·W with fixed K and N.  Selects and records the single kernel
+ * configuration (tile, instruction shape, pipeline depth, split count) from K, N, dtype,
+ * scale_layout and the current device's SM count; M is not an input.  Allocates a 4-byte
+ * device status word.  Requirements (else BI_GEMM_ERR_UNSUPPORTED): K >= 1, N >= 1,
+ * K, N < 2^31; bf16: K % 8 == 0 and N % 8 == 0 (16-byte row pitch); MXFP8: K % 128 == 0
+ * and N % 16 == 0, scale_layout == BI_SCALES_E8M0_K32; bf16: scale_layout == BI_SCALES_NONE.
+ * The device must be compute capability 10.3 (sm_103a).  On success *out owns the handle;
+ * release it with bi_gemm_destroy. */
+int bi_gemm_create(bi_gemm_t* out, int64_t K, int64_t N, int dtype, int scale_layout);
+
+/* Options for bi_gemm_create_ex.  Zero-initialise, then set what you need. */
+typedef struct {
+  int32_t split_k;        /* 0 = automatic (the rule above); >= 1 forces this fixed split
+                             count (1 <= split_k <= ceil(K / BK)); still never M-dependent */
+  int32_t max_ctas;       /* 0 = one CTA per SM; otherwise an upper bound on the grid     */
+  uint64_t timeout_ns;    /* 0 = default (5 s); limit of every in-kernel wait             */
+} bi_gemm_options;
+
+/* bi_gemm_create with explicit options (NULL = defaults, same as bi_gemm_create). */
+int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtype, int scale_layout,
+                      const bi_gemm_options* opt);
+
+/* Enqueue y = x·W on `stream`.  M >= 0 rows (M == 0 is a no-op that returns BI_GEMM_OK).
+ * x, W, y: device pointers, 16-byte aligned.  scales: NULL for bf16; for MXFP8 a host
+ * struct holding the two device scale pointers.  Asynchronous: returns after queuing.
+ * When the handle's split count is > 1 the handle grows its workspace (fp32 partials,
+ * tiles*S*128*BN*4 bytes, plus one arrival counter per tile) with stream-ordered
+ * allocation on `stream` the first time a larger M needs it; BI_GEMM_ERR_OOM if that fails.
+ * Errors from the kernel's bounded waits are reported by bi_gemm_get_device_error. */
+int bi_gemm_run(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                const bi_gemm_scales* scales, void* y, void* stream);
+
+/* Synchronise `stream`, then read and clear the handle's device status word: BI_GEMM_OK,
+ * or BI_GEMM_ERR_TIMEOUT if any run since the last call had a bounded wait expire (its
+ * output is then undefined), or BI_GEMM_ERR_CUDA if synchronisation failed. */
+int bi_gemm_get_device_error(bi_gemm_t h, void* stream);
+
+/* Release the handle, its status word and its workspace (synchronises the device first).
+ * NULL is accepted. */
+int bi_gemm_destroy(bi_gemm_t h);
+
+/* The fixed configuration recorded in a handle. */
+typedef struct {
+  int32_t block_m, block_n, block_k;  /* output tile rows / columns, K per pipeline stage  */
+  int32_t mma_m, mma_n, mma_k;        /* tcgen05.mma instruction shape                     */
+  int32_t stages;                     /* shared-memory pipeline depth                       */
+  int32_t split_k;                    /* S: fixed K split count (1 = none)                  */
+  int32_t num_sms;                    /* SMs on the device at create                        */
+  int32_t max_ctas;                   /* grid upper bound                                   */
+  int32_t threads;                    /* threads per CTA                                    */
+  int32_t smem_bytes;                 /* dynamic shared memory per CTA                      */
+  int32_t tmem_cols;                  /* tensor-memory columns per CTA                      */
+} bi_gemm_config;
+
+int bi_gemm_get_config(bi_gemm_t h, bi_gemm_config* cfg);
+
+/* Bytes of workspace a run with M rows needs on this handle (0 when split_k == 1). */
+int bi_gemm_workspace_size(bi_gemm_t h, int64_t M, uint64_t* bytes);
+
+/* Static description of an error code (never NULL). */
+const char* bi_gemm_strerror(int code);
+
+/* Library ABI version: (major << 16) | minor. */
+int bi_gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BI_GEMM_H */

@@ -1,0 +1,58 @@
+/*
+ * bi_gemm_controls.h — TEST-ONLY C ABI of libbi_gemm_controls.so.
+ *
+ * Deliberately batch-variant negative controls, for proving that the batch-invariance
+ * harness can fail, and a failure-injection hook for the bounded in-kernel waits.  The
+ * product library (bi_gemm.h) never contains or calls any of this.  Handles created here
+ * belong to this library only; do not pass them to libbi_gemm.so or vice versa.
+ *
+ * The two defects are those of "[BI][DSv4] Make mHC tilelang ops batch invariant"
+ * (github.com/aoshen02/vllm/pull/22, "What"): a K-split count derived from the token count,
+ * n_sms // cdiv(num_tokens, 64), and a second implementation used at num_tokens <= 16.
+ * Argument rules, layouts, ownership and return codes are those of bi_gemm.h.
+ */
+#ifndef BI_GEMM_CONTROLS_H
+#define BI_GEMM_CONTROLS_H
+
+#include <stdint.h>
+
+#include "bi_gemm.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* bi_gemm_create_ex with split_k (0 = automatic) and timeout_ns (0 = default). */
+int bi_ctl_create(bi_gemm_t* out, int64_t K, int64_t N, int dtype, int scale_layout,
+                  int32_t split_k, uint64_t timeout_ns);
+int bi_ctl_destroy(bi_gemm_t h);
+int bi_ctl_get_device_error(bi_gemm_t h, void* stream);
+
+/* The batch-invariant product path as compiled into this library. */
+int bi_ctl_run(bi_gemm_t h, const void* x, int64_t M, const void* W,
+               const bi_gemm_scales* scales, void* y, void* stream);
+
+/* Control N1: the split count used for M rows, n_sms / cdiv(M, 64) clamped to [1, KB]. */
+int bi_ctl_msplit_count(bi_gemm_t h, int64_t M);
+
+/* Control N1: run with that M-dependent split count (fixed-order merge, but the K ranges
+ * and hence the reduction tree change with M). */
+int bi_ctl_run_msplit(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                      const bi_gemm_scales* scales, void* y, void* stream);
+
+/* Control N2: M <= 16 runs a CUDA-core fp32 FMA kernel (ascending k), larger M the product
+ * kernel.  bf16 inputs only (BI_GEMM_ERR_UNSUPPORTED for MXFP8). */
+int bi_ctl_run_smallm_fork(bi_gemm_t h, const void* x, int64_t M, const void* W, void* y,
+                           void* stream);
+
+/* Failure injection: the TMA producer withholds the first stage of each CTA's first tile,
+ * so the MMA issuer's bounded wait expires.  The kernel records an error in the status word
+ * (read by bi_ctl_get_device_error as BI_GEMM_ERR_TIMEOUT), lets in-flight copies finish,
+ * frees its tensor memory and returns; y is undefined.  No GPU fault is raised. */
+int bi_ctl_run_stall(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                     const bi_gemm_scales* scales, void* y, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BI_GEMM_CONTROLS_H */

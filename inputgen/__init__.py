@@ -52,14 +52,25 @@ def splitmix64(seed: int, idx: np.ndarray) -> np.ndarray:
         return z ^ (z >> np.uint64(31))
 
 
-def normal(seed: int, start: int, count: int) -> np.ndarray:
-    """``count`` standard normal samples (fp64), stream elements start..start+count-1."""
+_CHUNK = 1 << 20
+
+
+def _normal_chunk(seed: int, start: int, count: int) -> np.ndarray:
     i = np.arange(start, start + count, dtype=np.uint64)
     w0 = splitmix64(seed, np.uint64(2) * i)
     w1 = splitmix64(seed, np.uint64(2) * i + np.uint64(1))
     u1 = ((w0 >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0**-53
     u2 = (w1 >> np.uint64(11)).astype(np.float64) * 2.0**-53
     return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+
+
+def normal(seed: int, start: int, count: int) -> np.ndarray:
+    """``count`` standard normal samples (fp64), stream elements start..start+count-1."""
+    out = np.empty(count, np.float64)
+    for c0 in range(0, count, _CHUNK):
+        c1 = min(count, c0 + _CHUNK)
+        out[c0:c1] = _normal_chunk(seed, start + c0, c1 - c0)
+    return out
 
 
 def uniform_int(seed: int, start: int, count: int, lo: int, hi: int) -> np.ndarray:
@@ -118,8 +129,12 @@ def to_e4m3_codes(v: np.ndarray) -> np.ndarray:
 
 def normal_bf16(seed: int, rows: int, cols: int, std: float = 1.0, row0: int = 0) -> np.ndarray:
     """[rows, cols] bf16 bit patterns of N(0, std^2), rows row0.. of the seed's stream."""
-    z = normal(seed, row0 * cols, rows * cols) * std
-    return to_bf16_bits(z).reshape(rows, cols)
+    n = rows * cols
+    out = np.empty(n, np.uint16)
+    for c0 in range(0, n, _CHUNK):
+        c1 = min(n, c0 + _CHUNK)
+        out[c0:c1] = to_bf16_bits(_normal_chunk(seed, row0 * cols + c0, c1 - c0) * std)
+    return out.reshape(rows, cols)
 
 
 def normal_e4m3(seed: int, rows: int, cols: int, row0: int = 0) -> np.ndarray:

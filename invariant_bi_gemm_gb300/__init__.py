@@ -1,0 +1,241 @@
+"""Python binding of the batch-invariant GEMM library (libbi_gemm.so, C ABI in include/bi_gemm.h).
+
+Argument marshalling only: every step of y = x·W runs in the CUDA kernels of
+``csrc/``.  PyTorch supplies device memory and streams.  There is no CPU or
+PyTorch fallback: importing this module fails if the library has not been built
+(``python -m invariant_bi_gemm_gb300.build``), and every call that the library
+refuses raises ``BiGemmError``.
+
+Low-level functions carry the C names (``bi_gemm_create``, ``bi_gemm_run``, ...)
+and take raw device pointers; ``BiGemm`` wraps them for torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+BI_BF16_OUT_BF16 = 0
+BI_BF16_OUT_F32 = 1
+BI_MXFP8E4M3_OUT_BF16 = 2
+BI_SCALES_NONE = 0
+BI_SCALES_E8M0_K32 = 1
+
+BI_GEMM_OK = 0
+BI_GEMM_ERR_INVALID_ARG = -1
+BI_GEMM_ERR_UNSUPPORTED = -2
+BI_GEMM_ERR_ALIGNMENT = -3
+BI_GEMM_ERR_CUDA = -4
+BI_GEMM_ERR_OOM = -5
+BI_GEMM_ERR_TIMEOUT = -6
+
+# every symbol include/bi_gemm.h declares
+EXPORTED_SYMBOLS = (
+    "bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_get_device_error",
+    "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_strerror",
+    "bi_gemm_version",
+)
+
+
+class BiGemmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {bi_gemm_strerror(code)} ({code})")
+
+
+class bi_gemm_scales(ctypes.Structure):
+    _fields_ = [("sx", ctypes.c_void_p), ("sw", ctypes.c_void_p)]
+
+
+class bi_gemm_options(ctypes.Structure):
+    _fields_ = [("split_k", ctypes.c_int32), ("max_ctas", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64)]
+
+
+class bi_gemm_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "block_m", "block_n", "block_k", "mma_m", "mma_n", "mma_k", "stages", "split_k",
+        "num_sms", "max_ctas", "threads", "smem_bytes", "tmem_cols")]
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.lib_path("libbi_gemm.so")
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: the CUDA library has not been built "
+            "(run `python -m invariant_bi_gemm_gb300.build`); there is no fallback path")
+    L = ctypes.CDLL(path)
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.bi_gemm_create.argtypes = [ctypes.POINTER(P), I64, I64, I32, I32]
+    L.bi_gemm_create_ex.argtypes = [ctypes.POINTER(P), I64, I64, I32, I32, ctypes.POINTER(bi_gemm_options)]
+    L.bi_gemm_run.argtypes = [P, P, I64, P, ctypes.POINTER(bi_gemm_scales), P, P]
+    L.bi_gemm_get_device_error.argtypes = [P, P]
+    L.bi_gemm_destroy.argtypes = [P]
+    L.bi_gemm_get_config.argtypes = [P, ctypes.POINTER(bi_gemm_config)]
+    L.bi_gemm_workspace_size.argtypes = [P, I64, ctypes.POINTER(ctypes.c_uint64)]
+    L.bi_gemm_strerror.argtypes = [I32]
+    L.bi_gemm_strerror.restype = ctypes.c_char_p
+    L.bi_gemm_version.argtypes = []
+    for n in ("bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_get_device_error",
+              "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_version"):
+        getattr(L, n).restype = I32
+    return L
+
+
+_lib = None
+LIB_PATH = _build.lib_path("libbi_gemm.so")
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libbi_gemm.so (loaded on first use; ImportError if it was never built)."""
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != BI_GEMM_OK:
+        raise BiGemmError(rc, where)
+
+
+# --------------------------------------------------------------------- C names
+
+def bi_gemm_strerror(code: int) -> str:
+    return library().bi_gemm_strerror(int(code)).decode()
+
+
+def bi_gemm_version() -> int:
+    return library().bi_gemm_version()
+
+
+def bi_gemm_create(K: int, N: int, dtype: int, scale_layout: int = BI_SCALES_NONE,
+                   options: bi_gemm_options | None = None) -> int:
+    """Returns the handle (an opaque integer); raises BiGemmError on refusal."""
+    h = ctypes.c_void_p()
+    if options is None:
+        rc = library().bi_gemm_create(ctypes.byref(h), int(K), int(N), int(dtype), int(scale_layout))
+    else:
+        rc = library().bi_gemm_create_ex(ctypes.byref(h), int(K), int(N), int(dtype), int(scale_layout),
+                                   ctypes.byref(options))
+    _check(rc, "bi_gemm_create")
+    return h.value
+
+
+def bi_gemm_run(h: int, x: int, M: int, W: int, scales: bi_gemm_scales | None, y: int, stream: int) -> None:
+    """Raw-pointer call: x, W, y device addresses, stream a cudaStream_t value."""
+    rc = library().bi_gemm_run(ctypes.c_void_p(h), ctypes.c_void_p(x), int(M), ctypes.c_void_p(W),
+                         ctypes.byref(scales) if scales is not None else None, ctypes.c_void_p(y),
+                         ctypes.c_void_p(stream))
+    _check(rc, "bi_gemm_run")
+
+
+def bi_gemm_get_device_error(h: int, stream: int = 0) -> int:
+    return library().bi_gemm_get_device_error(ctypes.c_void_p(h), ctypes.c_void_p(stream))
+
+
+def bi_gemm_destroy(h: int) -> None:
+    _check(library().bi_gemm_destroy(ctypes.c_void_p(h)), "bi_gemm_destroy")
+
+
+def bi_gemm_get_config(h: int) -> dict:
+    c = bi_gemm_config()
+    _check(library().bi_gemm_get_config(ctypes.c_void_p(h), ctypes.byref(c)), "bi_gemm_get_config")
+    return {n: getattr(c, n) for n, _ in bi_gemm_config._fields_}
+
+
+def bi_gemm_workspace_size(h: int, M: int) -> int:
+    b = ctypes.c_uint64()
+    _check(library().bi_gemm_workspace_size(ctypes.c_void_p(h), int(M), ctypes.byref(b)), "bi_gemm_workspace_size")
+    return b.value
+
+
+# --------------------------------------------------------------------- torch wrapper
+
+_DTYPES = {"bf16": BI_BF16_OUT_BF16, "bf16_f32": BI_BF16_OUT_F32, "mxfp8": BI_MXFP8E4M3_OUT_BF16}
+
+
+class BiGemm:
+    """y = x·W for fixed (K, N) on torch tensors.
+
+    kind: "bf16" (bf16 in/out), "bf16_f32" (bf16 in, fp32 out) or "mxfp8" (E4M3 codes as
+    uint8 / float8_e4m3fn tensors, E8M0 scales as uint8, bf16 out).
+    """
+
+    def __init__(self, K: int, N: int, kind: str = "bf16", split_k: int = 0, max_ctas: int = 0,
+                 timeout_ns: int = 0):
+        self.K, self.N, self.kind = int(K), int(N), kind
+        self.dtype = _DTYPES[kind]
+        layout = BI_SCALES_E8M0_K32 if kind == "mxfp8" else BI_SCALES_NONE
+        opts = None
+        if split_k or max_ctas or timeout_ns:
+            opts = bi_gemm_options(int(split_k), int(max_ctas), int(timeout_ns))
+        self.handle = bi_gemm_create(self.K, self.N, self.dtype, layout, opts)
+
+    @property
+    def config(self) -> dict:
+        return bi_gemm_get_config(self.handle)
+
+    def out_dtype(self):
+        import torch
+        return torch.float32 if self.kind == "bf16_f32" else torch.bfloat16
+
+    def run(self, x, W, y=None, sx=None, sw=None, stream=None):
+        import torch
+        M = int(x.shape[0])
+        if x.dim() != 2 or x.shape[1] != self.K or tuple(W.shape) != (self.K, self.N):
+            raise ValueError("shape mismatch: x [M, K], W [K, N] expected")
+        if not (x.is_cuda and W.is_cuda and x.is_contiguous() and W.is_contiguous()):
+            raise ValueError("x and W must be contiguous CUDA tensors")
+        want = torch.bfloat16 if self.kind != "mxfp8" else None
+        if want is not None and (x.dtype != want or W.dtype != want):
+            raise ValueError("bf16 inputs expected")
+        if want is None and (x.element_size() != 1 or W.element_size() != 1):
+            raise ValueError("E4M3 inputs (1 byte per element) expected")
+        if y is None:
+            y = torch.empty((M, self.N), dtype=self.out_dtype(), device=x.device)
+        if tuple(y.shape) != (M, self.N) or y.dtype != self.out_dtype() or not y.is_contiguous():
+            raise ValueError("y must be a contiguous [M, N] tensor of the output dtype")
+        scales = None
+        if self.kind == "mxfp8":
+            if sx is None or sw is None:
+                raise ValueError("MXFP8 needs sx [M, K/32] and sw [K/32, N] E8M0 tensors")
+            if tuple(sx.shape) != (M, self.K // 32) or tuple(sw.shape) != (self.K // 32, self.N):
+                raise ValueError("scale shapes: sx [M, K/32], sw [K/32, N]")
+            if sx.element_size() != 1 or sw.element_size() != 1 or not (sx.is_contiguous() and sw.is_contiguous()):
+                raise ValueError("scales must be contiguous uint8 tensors")
+            scales = bi_gemm_scales(sx.data_ptr(), sw.data_ptr())
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        bi_gemm_run(self.handle, x.data_ptr(), M, W.data_ptr(), scales, y.data_ptr(), s)
+        return y
+
+    __call__ = run
+
+    def device_error(self, stream=None) -> int:
+        s = 0
+        if stream is not None:
+            s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        return bi_gemm_get_device_error(self.handle, s)
+
+    def workspace_size(self, M: int) -> int:
+        return bi_gemm_workspace_size(self.handle, M)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            bi_gemm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+__all__ = [
+    "BiGemm", "BiGemmError", "bi_gemm_create", "bi_gemm_run", "bi_gemm_get_device_error",
+    "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_strerror",
+    "bi_gemm_version", "bi_gemm_scales", "bi_gemm_options", "EXPORTED_SYMBOLS", "LIB_PATH", "library",
+]

@@ -1,0 +1,421 @@
+// bi_gemm.cu — host side of the batch-invariant GEMM: configuration at create, tensor maps,
+// workspace, launch, status word.  Implements include/bi_gemm.h.
+//
+// The configuration rule ("Batch-invariant matrix multiplication", nondeterminism article:
+// compile one kernel configuration and use it for all shapes; strategy switches keyed on
+// the block/SM ratio are where libraries lose invariance):
+//   tile      128 x BN, BN = 64 / 128 / 256 (bf16) or 128 / 256 (MXFP8) from N alone;
+//   MMA       tcgen05.mma M=128, N=BN, K=16 (bf16) or K=32 (MXFP8 block-scaled);
+//   K stage   128 bytes of K per stage (64 bf16 / 128 E4M3), ascending k-blocks;
+//   split S   1, except for a single N tile (N <= BN) with a long K, where
+//             S = min(32, pow2floor(SMs / 4), pow2floor(KB / 8)) — the pinned
+//             "min(cap, n_sms // 4) rounded down to a power of two" of "[BI][DSv4] Make mHC
+//             tilelang ops batch invariant" ("What"), with each split keeping >= 8 k-blocks.
+// None of these reads M.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/bi_gemm.h"
+#include "bi_gemm_kernel.cuh"
+
+#ifndef BI_GEMM_API
+#define BI_GEMM_API extern "C" __attribute__((visibility("default")))
+#endif
+
+namespace bigemm {
+
+constexpr int kVersion = (1 << 16) | 0;
+constexpr uint64_t kDefaultTimeoutNs = 5ull * 1000 * 1000 * 1000;
+
+// ------------------------------------------------------------------ kernel table
+
+struct KernelInfo {
+  const void* fn = nullptr;
+  int threads = 0, smem = 0, tmem_cols = 0, stages = 0, bn = 0, bk = 0, mma_k = 0;
+};
+
+template <class C>
+KernelInfo info_of() {
+  KernelInfo k;
+  k.fn = reinterpret_cast<const void*>(&bi_gemm_kernel<C>);
+  k.threads = C::THREADS;
+  k.smem = C::SMEM_BYTES;
+  k.tmem_cols = C::TMEM_COLS;
+  k.stages = C::STAGES;
+  k.bn = C::BN;
+  k.bk = C::BK;
+  k.mma_k = C::MMA_K;
+  return k;
+}
+
+// dtype 0/1: bf16 in, bf16/f32 out; dtype 2: MXFP8 in, bf16 out.
+static KernelInfo select_kernel(int dtype, int bn) {
+  switch (dtype) {
+    case BI_BF16_OUT_BF16:
+      if (bn == 64) return info_of<KCfg<false, false, 64, 8, 2>>();
+      if (bn == 128) return info_of<KCfg<false, false, 128, 6, 2>>();
+      return info_of<KCfg<false, false, 256, 4, 2>>();
+    case BI_BF16_OUT_F32:
+      if (bn == 64) return info_of<KCfg<false, true, 64, 8, 2>>();
+      if (bn == 128) return info_of<KCfg<false, true, 128, 6, 2>>();
+      return info_of<KCfg<false, true, 256, 4, 2>>();
+    default:
+      if (bn == 128) return info_of<KCfg<true, false, 128, 6, 2>>();
+      return info_of<KCfg<true, false, 256, 4, 1>>();
+  }
+}
+
+static int pow2_floor(int64_t v) {
+  int p = 1;
+  while ((int64_t)p * 2 <= v) p *= 2;
+  return v >= 1 ? p : 0;
+}
+
+// ------------------------------------------------------------------ tensor-map encoder
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major [rows, cols] tensor, box [box_rows, box_cols], 128-byte swizzle, zero fill.
+static bool encode_2d(CUtensorMap* m, const void* base, bool u8, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows, uint32_t box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t elem = u8 ? 1 : 2;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * elem};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace bigemm
+
+using namespace bigemm;
+
+struct bi_gemm {
+  int64_t K = 0, N = 0;
+  int dtype = 0, scale_layout = 0;
+  int device = 0, num_sms = 0, max_ctas = 0;
+  int split = 1, kblocks = 0, n_tiles = 0;
+  uint64_t timeout_ns = kDefaultTimeoutNs;
+  KernelInfo kern;
+  uint32_t* d_status = nullptr;
+  // split-K workspace: [arrival counters, cap_tiles x 4 B, padded to 256 B][fp32 partials]
+  void* ws = nullptr;
+  int64_t ws_cap_tiles = 0;
+  size_t ws_cap_part = 0;
+  bool ws_dirty = false;
+  // W tensor map cache
+  const void* w_cached = nullptr;
+  CUtensorMap tmap_w;
+  std::mutex mu;
+};
+
+namespace {
+
+bool is_aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shape(int64_t K, int64_t N, int dtype, int scale_layout) {
+  if (dtype < BI_BF16_OUT_BF16 || dtype > BI_MXFP8E4M3_OUT_BF16) return BI_GEMM_ERR_INVALID_ARG;
+  if (scale_layout != BI_SCALES_NONE && scale_layout != BI_SCALES_E8M0_K32)
+    return BI_GEMM_ERR_INVALID_ARG;
+  if (K < 0 || N < 0) return BI_GEMM_ERR_INVALID_ARG;
+  if (K == 0 || N == 0 || K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+    return BI_GEMM_ERR_UNSUPPORTED;
+  if (dtype == BI_MXFP8E4M3_OUT_BF16) {
+    if (scale_layout != BI_SCALES_E8M0_K32) return BI_GEMM_ERR_UNSUPPORTED;
+    if (K % 128 != 0 || N % 16 != 0) return BI_GEMM_ERR_UNSUPPORTED;
+  } else {
+    if (scale_layout != BI_SCALES_NONE) return BI_GEMM_ERR_UNSUPPORTED;
+    if (K % 8 != 0 || N % 8 != 0) return BI_GEMM_ERR_UNSUPPORTED;
+  }
+  return BI_GEMM_OK;
+}
+
+int block_n_for(int64_t N, int dtype) {
+  if (dtype == BI_MXFP8E4M3_OUT_BF16) return N <= 128 ? 128 : 256;
+  return N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+}
+
+int auto_split(int64_t n_tiles, int64_t kblocks, int num_sms) {
+  if (n_tiles != 1) return 1;
+  int s = std::min(32, std::min(pow2_floor(num_sms / 4), pow2_floor(kblocks / 8)));
+  return std::max(1, s);
+}
+
+size_t counters_bytes(int64_t tiles) { return (size_t(tiles) * sizeof(uint32_t) + 255) & ~size_t(255); }
+
+// Make the workspace hold `tiles` counters (all zero) and tiles*split partial tiles.
+int ensure_workspace(bi_gemm* h, int64_t tiles, int split, cudaStream_t st) {
+  if (split <= 1) return BI_GEMM_OK;
+  const size_t part = size_t(tiles) * split * kBM * h->kern.bn * sizeof(float);
+  if (h->ws && tiles <= h->ws_cap_tiles && part <= h->ws_cap_part) {
+    if (h->ws_dirty) {
+      if (cudaMemsetAsync(h->ws, 0, counters_bytes(h->ws_cap_tiles), st) != cudaSuccess)
+        return BI_GEMM_ERR_CUDA;
+      h->ws_dirty = false;
+    }
+    return BI_GEMM_OK;
+  }
+  const int64_t cap_tiles = std::max(tiles, h->ws_cap_tiles);
+  const size_t cap_part = std::max(part, h->ws_cap_part);
+  if (h->ws) {
+    cudaFreeAsync(h->ws, st);
+    h->ws = nullptr;
+    h->ws_cap_tiles = 0;
+    h->ws_cap_part = 0;
+  }
+  void* p = nullptr;
+  if (cudaMallocAsync(&p, counters_bytes(cap_tiles) + cap_part, st) != cudaSuccess) {
+    cudaGetLastError();
+    return BI_GEMM_ERR_OOM;
+  }
+  if (cudaMemsetAsync(p, 0, counters_bytes(cap_tiles), st) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFreeAsync(p, st);
+    return BI_GEMM_ERR_CUDA;
+  }
+  h->ws = p;
+  h->ws_cap_tiles = cap_tiles;
+  h->ws_cap_part = cap_part;
+  h->ws_dirty = false;
+  return BI_GEMM_OK;
+}
+
+// Launch one run; `split_override` > 0 replaces the handle's split count (control build only).
+int launch(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_gemm_scales* scales,
+           void* y, cudaStream_t st, int split_override, uint32_t test_flags) {
+  const bool fp8 = h->dtype == BI_MXFP8E4M3_OUT_BF16;
+  const int split = split_override > 0 ? split_override : h->split;
+  const int64_t m_tiles = (M + kBM - 1) / kBM;
+  const int64_t tiles = m_tiles * h->n_tiles;
+  if (tiles * split >= (int64_t(1) << 31)) return BI_GEMM_ERR_UNSUPPORTED;
+
+  CUtensorMap tmap_x;
+  if (!encode_2d(&tmap_x, x, fp8, uint64_t(M), uint64_t(h->K), kBM, 128 / (fp8 ? 1 : 2)))
+    return BI_GEMM_ERR_CUDA;
+  if (h->w_cached != W) {
+    if (!encode_2d(&h->tmap_w, W, fp8, uint64_t(h->K), uint64_t(h->N), h->kern.bk,
+                   128 / (fp8 ? 1 : 2))) {
+      h->w_cached = nullptr;
+      return BI_GEMM_ERR_CUDA;
+    }
+    h->w_cached = W;
+  }
+
+  int rc = ensure_workspace(h, tiles, split, st);
+  if (rc != BI_GEMM_OK) return rc;
+
+  KParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.y = y;
+  p.sx = scales ? scales->sx : nullptr;
+  p.sw = scales ? scales->sw : nullptr;
+  p.counters = split > 1 ? static_cast<uint32_t*>(h->ws) : nullptr;
+  p.ws = split > 1 ? reinterpret_cast<float*>(static_cast<char*>(h->ws) + counters_bytes(h->ws_cap_tiles))
+                   : nullptr;
+  p.status = h->d_status;
+  p.M = int32_t(M);
+  p.N = int32_t(h->N);
+  p.K = int32_t(h->K);
+  p.m_tiles = int32_t(m_tiles);
+  p.n_tiles = int32_t(h->n_tiles);
+  p.splits = split;
+  p.kblocks = h->kblocks;
+  p.timeout_ns = h->timeout_ns;
+  p.test_flags = test_flags;
+
+  const int64_t units = tiles * split;
+  const int grid = int(std::min<int64_t>(units, h->max_ctas));
+  void* args[3] = {&tmap_x, &h->tmap_w, &p};
+  cudaError_t e = cudaLaunchKernel(h->kern.fn, dim3(grid), dim3(h->kern.threads), args,
+                                   size_t(h->kern.smem), st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return BI_GEMM_ERR_CUDA;
+  }
+  return BI_GEMM_OK;
+}
+
+int validate_run(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_gemm_scales* scales,
+                 void* y) {
+  if (!h || M < 0) return BI_GEMM_ERR_INVALID_ARG;
+  if (M == 0) return BI_GEMM_OK;
+  if (M >= (int64_t(1) << 31)) return BI_GEMM_ERR_UNSUPPORTED;
+  if (!x || !W || !y) return BI_GEMM_ERR_INVALID_ARG;
+  if (!is_aligned(x, 16) || !is_aligned(W, 16) || !is_aligned(y, 16)) return BI_GEMM_ERR_ALIGNMENT;
+  if (h->dtype == BI_MXFP8E4M3_OUT_BF16) {
+    if (!scales || !scales->sx || !scales->sw) return BI_GEMM_ERR_INVALID_ARG;
+    if (!is_aligned(scales->sx, 4)) return BI_GEMM_ERR_ALIGNMENT;
+  } else if (scales && (scales->sx || scales->sw)) {
+    return BI_GEMM_ERR_INVALID_ARG;
+  }
+  return BI_GEMM_OK;
+}
+
+}  // namespace
+
+BI_GEMM_API int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtype,
+                                  int scale_layout, const bi_gemm_options* opt) {
+  if (!out) return BI_GEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = check_shape(K, N, dtype, scale_layout);
+  if (rc != BI_GEMM_OK) return rc;
+  const int bn = block_n_for(N, dtype);
+  const int bk = dtype == BI_MXFP8E4M3_OUT_BF16 ? 128 : 64;
+  const int64_t kblocks = (K + bk - 1) / bk;
+  const int64_t n_tiles = (N + bn - 1) / bn;
+  if (opt && (opt->split_k < 0 || opt->split_k > kblocks || opt->max_ctas < 0))
+    return BI_GEMM_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return BI_GEMM_ERR_CUDA;
+  }
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return BI_GEMM_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return BI_GEMM_ERR_UNSUPPORTED;
+  if (!encode_fn()) return BI_GEMM_ERR_CUDA;
+
+  bi_gemm* h = new (std::nothrow) bi_gemm();
+  if (!h) return BI_GEMM_ERR_OOM;
+  h->K = K;
+  h->N = N;
+  h->dtype = dtype;
+  h->scale_layout = scale_layout;
+  h->device = dev;
+  h->num_sms = sms;
+  h->max_ctas = (opt && opt->max_ctas > 0) ? std::min(opt->max_ctas, sms) : sms;
+  h->kern = select_kernel(dtype, bn);
+  h->kblocks = int(kblocks);
+  h->n_tiles = int(n_tiles);
+  h->split = (opt && opt->split_k > 0) ? opt->split_k : auto_split(n_tiles, kblocks, sms);
+  h->timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+  if (cudaFuncSetAttribute(h->kern.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->kern.smem) !=
+          cudaSuccess ||
+      cudaMalloc(&h->d_status, sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(h->d_status, 0, sizeof(uint32_t)) != cudaSuccess) {
+    cudaGetLastError();
+    if (h->d_status) cudaFree(h->d_status);
+    delete h;
+    return BI_GEMM_ERR_CUDA;
+  }
+  *out = h;
+  return BI_GEMM_OK;
+}
+
+BI_GEMM_API int bi_gemm_create(bi_gemm_t* out, int64_t K, int64_t N, int dtype, int scale_layout) {
+  return bi_gemm_create_ex(out, K, N, dtype, scale_layout, nullptr);
+}
+
+BI_GEMM_API int bi_gemm_run(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                            const bi_gemm_scales* scales, void* y, void* stream) {
+  int rc = validate_run(h, x, M, W, scales, y);
+  if (rc != BI_GEMM_OK || M == 0) return rc;
+  std::lock_guard<std::mutex> lk(h->mu);
+  return launch(h, x, M, W, scales, y, static_cast<cudaStream_t>(stream), 0, 0u);
+}
+
+BI_GEMM_API int bi_gemm_get_device_error(bi_gemm_t h, void* stream) {
+  if (!h) return BI_GEMM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(h->mu);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemcpy(&v, h->d_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return BI_GEMM_ERR_CUDA;
+  }
+  if (v != 0) {
+    if (cudaMemset(h->d_status, 0, sizeof(uint32_t)) != cudaSuccess) {
+      cudaGetLastError();
+      return BI_GEMM_ERR_CUDA;
+    }
+    h->ws_dirty = true;   // an aborted split run may leave arrival counters non-zero
+    return BI_GEMM_ERR_TIMEOUT;
+  }
+  return BI_GEMM_OK;
+}
+
+BI_GEMM_API int bi_gemm_destroy(bi_gemm_t h) {
+  if (!h) return BI_GEMM_OK;
+  cudaDeviceSynchronize();
+  if (h->ws) cudaFree(h->ws);
+  if (h->d_status) cudaFree(h->d_status);
+  cudaGetLastError();
+  delete h;
+  return BI_GEMM_OK;
+}
+
+BI_GEMM_API int bi_gemm_get_config(bi_gemm_t h, bi_gemm_config* c) {
+  if (!h || !c) return BI_GEMM_ERR_INVALID_ARG;
+  c->block_m = kBM;
+  c->block_n = h->kern.bn;
+  c->block_k = h->kern.bk;
+  c->mma_m = kBM;
+  c->mma_n = h->kern.bn;
+  c->mma_k = h->kern.mma_k;
+  c->stages = h->kern.stages;
+  c->split_k = h->split;
+  c->num_sms = h->num_sms;
+  c->max_ctas = h->max_ctas;
+  c->threads = h->kern.threads;
+  c->smem_bytes = h->kern.smem;
+  c->tmem_cols = h->kern.tmem_cols;
+  return BI_GEMM_OK;
+}
+
+BI_GEMM_API int bi_gemm_workspace_size(bi_gemm_t h, int64_t M, uint64_t* bytes) {
+  if (!h || !bytes || M < 0) return BI_GEMM_ERR_INVALID_ARG;
+  if (h->split <= 1 || M == 0) {
+    *bytes = 0;
+    return BI_GEMM_OK;
+  }
+  const int64_t tiles = ((M + kBM - 1) / kBM) * h->n_tiles;
+  *bytes = counters_bytes(tiles) + size_t(tiles) * h->split * kBM * h->kern.bn * sizeof(float);
+  return BI_GEMM_OK;
+}
+
+BI_GEMM_API const char* bi_gemm_strerror(int code) {
+  switch (code) {
+    case BI_GEMM_OK: return "ok";
+    case BI_GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case BI_GEMM_ERR_UNSUPPORTED: return "unsupported shape, dtype or device";
+    case BI_GEMM_ERR_ALIGNMENT: return "pointer or row pitch not 16-byte aligned";
+    case BI_GEMM_ERR_CUDA: return "CUDA runtime error";
+    case BI_GEMM_ERR_OOM: return "workspace allocation failed";
+    case BI_GEMM_ERR_TIMEOUT: return "bounded in-kernel wait expired";
+    default: return "unknown error code";
+  }
+}
+
+BI_GEMM_API int bi_gemm_version(void) { return kVersion; }

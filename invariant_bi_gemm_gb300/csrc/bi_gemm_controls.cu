@@ -1,0 +1,112 @@
+// bi_gemm_controls.cu — TEST-ONLY library libbi_gemm_controls.so: deliberately batch-variant
+// negative controls and a failure-injection hook.  Never loaded by the product path.
+//
+// The controls reproduce the two defects of "[BI][DSv4] Make mHC tilelang ops batch
+// invariant" ("What"): a K-split count derived from the token count
+// (n_sms // cdiv(num_tokens, 64)), which changes the reduction tree with the batch, and a
+// second implementation for num_tokens <= 16.  The batch-invariance harness must report
+// non-zero byte diffs for both, otherwise it could not tell a broken kernel from a good one
+// ("Tests" on the same page: negative controls that actually fail).
+//
+// The product code is compiled in with its C entry points hidden, so this library's
+// bi_ctl_* functions use their own copies and never mix handles with libbi_gemm.so.
+#define BI_GEMM_CONTROLS 1
+#define BI_GEMM_API extern "C" __attribute__((visibility("hidden")))
+#include "bi_gemm.cu"
+
+#include <cuda_bf16.h>
+
+#include "../../include/bi_gemm_controls.h"
+
+#define BI_CTL_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+// Second implementation for small batches: one thread per output, fp32 fused multiply-add
+// in ascending k on the CUDA cores (a different rounding sequence from the tensor cores).
+template <bool kOutF32>
+__global__ void small_m_fma_kernel(const __nv_bfloat16* __restrict__ x,
+                                   const __nv_bfloat16* __restrict__ w, void* __restrict__ y,
+                                   int M, int N, int K) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = blockIdx.y;
+  if (i >= M || j >= N) return;
+  float acc = 0.f;
+  for (int k = 0; k < K; ++k)
+    acc = fmaf(__bfloat162float(x[(size_t)i * K + k]), __bfloat162float(w[(size_t)k * N + j]), acc);
+  if (kOutF32)
+    reinterpret_cast<float*>(y)[(size_t)i * N + j] = acc;
+  else
+    reinterpret_cast<__nv_bfloat16*>(y)[(size_t)i * N + j] = __float2bfloat16_rn(acc);
+}
+
+}  // namespace
+
+BI_CTL_API int bi_ctl_create(bi_gemm_t* out, int64_t K, int64_t N, int dtype, int scale_layout,
+                             int32_t split_k, uint64_t timeout_ns) {
+  bi_gemm_options o;
+  std::memset(&o, 0, sizeof(o));
+  o.split_k = split_k;
+  o.timeout_ns = timeout_ns;
+  return bi_gemm_create_ex(out, K, N, dtype, scale_layout, &o);
+}
+
+BI_CTL_API int bi_ctl_destroy(bi_gemm_t h) { return bi_gemm_destroy(h); }
+
+BI_CTL_API int bi_ctl_get_device_error(bi_gemm_t h, void* stream) {
+  return bi_gemm_get_device_error(h, stream);
+}
+
+// The product path, as compiled into this library (reference for the controls).
+BI_CTL_API int bi_ctl_run(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                          const bi_gemm_scales* scales, void* y, void* stream) {
+  return bi_gemm_run(h, x, M, W, scales, y, stream);
+}
+
+// N1: split count = n_sms // cdiv(M, 64), clamped to [1, KB] — an M-dependent reduction tree.
+BI_CTL_API int bi_ctl_msplit_count(bi_gemm_t h, int64_t M) {
+  if (!h || M <= 0) return 0;
+  int64_t s = h->num_sms / ((M + 63) / 64);
+  s = std::max<int64_t>(1, std::min<int64_t>(s, h->kblocks));
+  return int(s);
+}
+
+BI_CTL_API int bi_ctl_run_msplit(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                                 const bi_gemm_scales* scales, void* y, void* stream) {
+  int rc = validate_run(h, x, M, W, scales, y);
+  if (rc != BI_GEMM_OK || M == 0) return rc;
+  std::lock_guard<std::mutex> lk(h->mu);
+  return launch(h, x, M, W, scales, y, static_cast<cudaStream_t>(stream),
+                bi_ctl_msplit_count(h, M), 0u);
+}
+
+// N2: M <= 16 goes to the CUDA-core kernel above; larger M to the product kernel.
+BI_CTL_API int bi_ctl_run_smallm_fork(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                                      void* y, void* stream) {
+  int rc = validate_run(h, x, M, W, nullptr, y);
+  if (rc != BI_GEMM_OK || M == 0) return rc;
+  if (h->dtype == BI_MXFP8E4M3_OUT_BF16) return BI_GEMM_ERR_UNSUPPORTED;
+  if (M > 16) return bi_gemm_run(h, x, M, W, nullptr, y, stream);
+  dim3 grid(unsigned((h->N + 127) / 128), unsigned(M));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (h->dtype == BI_BF16_OUT_F32)
+    small_m_fma_kernel<true><<<grid, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
+                                                   static_cast<const __nv_bfloat16*>(W), y, int(M),
+                                                   int(h->N), int(h->K));
+  else
+    small_m_fma_kernel<false><<<grid, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
+                                                    static_cast<const __nv_bfloat16*>(W), y, int(M),
+                                                    int(h->N), int(h->K));
+  return cudaGetLastError() == cudaSuccess ? BI_GEMM_OK : BI_GEMM_ERR_CUDA;
+}
+
+// Failure injection: the producer withholds the first stage of each CTA's first tile, so the
+// MMA issuer's bounded wait expires; the kernel must record BI_GEMM_ERR_TIMEOUT, drain, free
+// its tensor memory and return, leaving the context usable.
+BI_CTL_API int bi_ctl_run_stall(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                                const bi_gemm_scales* scales, void* y, void* stream) {
+  int rc = validate_run(h, x, M, W, scales, y);
+  if (rc != BI_GEMM_OK || M == 0) return rc;
+  std::lock_guard<std::mutex> lk(h->mu);
+  return launch(h, x, M, W, scales, y, static_cast<cudaStream_t>(stream), 0, 1u);
+}

@@ -1,0 +1,537 @@
+// bi_gemm_kernel.cuh — the batch-invariant GEMM kernel for sm_103a (TMA + tcgen05 + TMEM).
+//
+// y[M,N] = x[M,K] · W[K,N], fp32 accumulation, one compiled configuration per handle.
+//
+// Why this is batch invariant ("Batch-invariant matrix multiplication", nondeterminism
+// article: the three breakers are M-dependent split-K, stream-K and a smaller tensor-core
+// instruction at small M; the cure is one kernel configuration for every shape):
+//   * the output tile is always 128 x BN, the tcgen05 instruction always
+//     M=128 x N=BN x K=16 (bf16) or K=32 (MXFP8), whatever M is;
+//   * every output element is reduced over k-blocks kb = 0 .. KB-1 in ascending order, and
+//     within a k-block over the same fixed sequence of MMA instructions;
+//   * a split count S > 1 is fixed when the handle is created (from K, N and the SM count,
+//     never M); split s always covers k-blocks [s*KB/S, (s+1)*KB/S), and the S fp32
+//     partials are merged in the fixed serial order ((p0 + p1) + p2) + ... by whichever
+//     CTA arrives last (an integer arrival counter; no floating-point atomics);
+//   * rows beyond M are zero-filled by TMA and never stored; a row's products never meet
+//     another row's, so neither M nor the other rows' contents can reach row i.
+// The persistent tile order (which SM computes which tile, and when) does change with M,
+// but it decides no arithmetic: a tile's value is the same wherever it runs.
+//
+// Warp roles (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: x tile [128 x BK] (K-major, 128-byte swizzle) and W tile
+//               [BK x BN] (N-major, 128-byte swizzle) per pipeline stage;
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
+//   warp 2      (MXFP8 only) scale producer: E8M0 scales into the tcgen05.cp layout;
+//   last 4      epilogue: tcgen05.ld -> round to nearest even -> 16-byte global stores,
+//               or fp32 partials + ordered merge when S > 1.
+// Every wait is bounded in time; on expiry the kernel records an error bit in the
+// handle's status word, lets in-flight copies and MMAs finish, frees TMEM and returns.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace bigemm {
+
+constexpr int kBM = 128;
+
+// Error bits written to the status word (any non-zero value is reported as a timeout).
+enum : uint32_t {
+  kErrTimeoutProducer = 1u,
+  kErrTimeoutMma = 2u,
+  kErrTimeoutEpilogue = 4u,
+  kErrTimeoutScales = 8u,
+};
+
+struct KParams {
+  void* y;                  // [M, N] bf16 or fp32, row-major
+  const uint8_t* sx;        // MXFP8: [M, K/32] E8M0
+  const uint8_t* sw;        // MXFP8: [K/32, N] E8M0
+  float* ws;                // split-K partials [tiles][S][128][BN] fp32 (S > 1)
+  uint32_t* counters;       // split-K arrival counters [tiles] (S > 1)
+  uint32_t* status;         // error word
+  int32_t M, N, K;
+  int32_t m_tiles, n_tiles;
+  int32_t splits;           // S
+  int32_t kblocks;          // KB = ceil(K / BK)
+  uint64_t timeout_ns;
+  uint32_t test_flags;      // only read by the control build
+};
+
+constexpr __host__ __device__ int pow2_ceil(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <bool kFp8_, bool kOutF32_, int kBN_, int kStages_, int kAccBufs_>
+struct KCfg {
+  static constexpr bool kFp8 = kFp8_;
+  static constexpr bool kOutF32 = kOutF32_;
+  static constexpr int BN = kBN_;
+  static constexpr int STAGES = kStages_;
+  static constexpr int ACC_BUFS = kAccBufs_;
+  static constexpr int ELEM = kFp8 ? 1 : 2;
+  static constexpr int BK = 128 / ELEM;                 // one 128-byte swizzle row of K
+  static constexpr int MMA_K = kFp8 ? 32 : 16;          // K per tcgen05.mma
+  static constexpr int K_STEPS = BK / MMA_K;            // 4
+  static constexpr int ATOM_N = 128 / ELEM;             // N per 128-byte swizzle row of W
+  static constexpr int N_ATOMS = BN / ATOM_N;
+  static_assert(BN % ATOM_N == 0 && BN >= 16 && BN <= 256, "BN");
+  static constexpr int A_BYTES = kBM * 128;             // 16 KB
+  static constexpr int B_ATOM_BYTES = BK * 128;
+  static constexpr int B_BYTES = N_ATOMS * B_ATOM_BYTES;
+  static constexpr int SFA_BYTES = kFp8 ? 512 : 0;      // 128 rows x 4 k-blocks
+  static constexpr int SFB_BYTES = kFp8 ? (BN / 128) * 512 : 0;
+  static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
+  static constexpr int NUM_WARPS = kFp8 ? 7 : 6;
+  static constexpr int EPI_WARP0 = NUM_WARPS - 4;
+  static constexpr int THREADS = NUM_WARPS * 32;
+  static constexpr int TX_BYTES = A_BYTES + B_BYTES;
+  // TMEM columns: accumulators first, then 16 columns of scale factors per stage.
+  static constexpr int SF_TMEM_COL0 = ACC_BUFS * BN;
+  static constexpr int TMEM_USED = SF_TMEM_COL0 + (kFp8 ? 16 * STAGES : 0);
+  static constexpr int TMEM_COLS = pow2_ceil(TMEM_USED < 32 ? 32 : TMEM_USED);
+  static_assert(TMEM_COLS <= 512, "TMEM");
+  // shared memory offsets from a 1024-byte aligned base
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+  // tcgen05 instruction descriptor (kind::f16): D=f32, A=B=bf16, A K-major, B N-major.
+  static constexpr uint32_t IDESC_BF16 =
+      (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
+      (uint32_t(BN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+  // tcgen05 instruction descriptor (kind::mxf8f6f4 block-scaled): A=B=E4M3, A K-major,
+  // B N-major, E8M0 scales; the scale-factor byte selectors are OR-ed in per K step.
+  static constexpr uint32_t IDESC_MXF8 =
+      (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) | (uint32_t(BN >> 3) << 17) |
+      (1u << 23) | (uint32_t(kBM >> 4) << 24);
+};
+
+// Shared-memory matrix descriptor: start, leading / stride byte offsets, version 1, layout.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                               uint32_t layout) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (uint64_t(layout) << 61);
+}
+constexpr uint32_t kLayoutNone = 0;
+constexpr uint32_t kLayoutSW128 = 2;
+
+struct SyncCtx {
+  volatile uint32_t* abort;  // shared: set once any role gives up
+  uint32_t* status;          // global error word
+  uint64_t timeout_ns;
+};
+
+// Bounded wait on an mbarrier phase.  Returns false (and raises the abort flag and the error
+// bit) once the time limit passes, or as soon as another role has aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const SyncCtx& c,
+                                           uint32_t err_bit) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*c.abort) return false;
+      if (ptx::globaltimer() - t0 > c.timeout_ns) {
+        *c.abort = 1u;
+        atomicOr(c.status, err_bit);
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, and on success every
+// lane observes the (already completed) phase itself before touching the guarded data.
+__device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, const SyncCtx& c,
+                                                uint32_t err_bit) {
+  const int lane = threadIdx.x & 31;
+  uint32_t ok = 1;
+  if (lane == 0) ok = wait_phase(bar, parity, c, err_bit) ? 1u : 0u;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) {
+    for (int i = 0; i < (1 << 20) && !ptx::mbar_try_wait(bar, parity); ++i) {
+    }
+  }
+  return ok != 0;
+}
+
+struct UnitCoord {
+  int tile, s, m_tile, n_tile, kb_begin, kb_end;
+};
+
+__device__ __forceinline__ UnitCoord unit_coord(int u, const KParams& p) {
+  UnitCoord c;
+  c.tile = u / p.splits;
+  c.s = u - c.tile * p.splits;
+  c.m_tile = c.tile % p.m_tiles;
+  c.n_tile = c.tile / p.m_tiles;
+  c.kb_begin = int((int64_t)c.s * p.kblocks / p.splits);
+  c.kb_end = int((int64_t)(c.s + 1) * p.kblocks / p.splits);
+  return c;
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    bi_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                   const __grid_constant__ CUtensorMap tmap_w, const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + C::ACC_BUFS + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::ACC_BUFS);
+  const uint32_t epi_bar = drain_bar + 8u;   // split-K hand-off among the 4 epilogue warps
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  uint32_t* tmem_slot = misc + 0;
+  volatile uint32_t* abort_flag = misc + 1;
+  volatile uint32_t* last_flag = misc + 2;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int units = p.m_tiles * p.n_tiles * p.splits;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), C::kFp8 ? 2u : 1u);
+      ptx::mbar_init(empty_bar(s), 1u);
+    }
+    for (int b = 0; b < C::ACC_BUFS; ++b) {
+      ptx::mbar_init(tfull_bar(b), 1u);
+      ptx::mbar_init(tempty_bar(b), 4u);
+    }
+    ptx::mbar_init(drain_bar, 1u);
+    ptx::mbar_init(epi_bar, 4u);
+    *abort_flag = 0u;
+    *last_flag = 0u;
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+    ptx::prefetch_tensormap(&tmap_x);
+    ptx::prefetch_tensormap(&tmap_w);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const SyncCtx sc{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_par = 0;   // per stage: an issue is outstanding / its parity
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const UnitCoord uc = unit_coord(u, p);
+        for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
+          if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          bool skip = false;
+#ifdef BI_GEMM_CONTROLS
+          // control build only: withhold one stage so that the consumer's bounded wait expires
+          skip = (p.test_flags & 1u) && u == (int)blockIdx.x && kb == uc.kb_begin;
+#endif
+          if (!skip) {
+            const uint32_t fb = full_bar(stage);
+            ptx::mbar_arrive_expect_tx(fb, C::TX_BYTES);
+            ptx::tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmap_x, fb, kb * C::BK,
+                             uc.m_tile * kBM);
+            const uint32_t bdst = sbase + C::OFF_B + stage * C::B_BYTES;
+#pragma unroll
+            for (int a = 0; a < C::N_ATOMS; ++a)
+              ptx::tma_load_2d(bdst + a * C::B_ATOM_BYTES, &tmap_w, fb,
+                               uc.n_tile * C::BN + a * C::ATOM_N, kb * C::BK);
+            issued_mask |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy already in flight land before the CTA can exit
+        SyncCtx drain{abort_flag, p.status, p.timeout_ns};
+        volatile uint32_t no_abort = 0;
+        drain.abort = &no_abort;
+        for (int s = 0; s < C::STAGES; ++s)
+          if (issued_mask & (1u << s))
+            wait_phase(full_bar(s), (issued_par >> s) & 1u, drain, kErrTimeoutProducer);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t bphase = 0;
+      bool ok = true, issued_any = false;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const UnitCoord uc = unit_coord(u, p);
+        if (!wait_phase(tempty_bar(buf), bphase ^ 1u, sc, kErrTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(buf * C::BN);
+        for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
+          if (!wait_phase(full_bar(stage), phase, sc, kErrTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = sbase + C::OFF_A + stage * C::A_BYTES;
+          const uint32_t b_addr = sbase + C::OFF_B + stage * C::B_BYTES;
+          if constexpr (C::kFp8) {
+            const uint32_t sf_addr = sbase + C::OFF_SF + stage * C::SF_BYTES;
+            const uint32_t sfa_t = tmem_base + uint32_t(C::SF_TMEM_COL0 + 16 * stage);
+            const uint32_t sfb_t = sfa_t + 8u;
+            ptx::tc_cp_32x128b_x4(sfa_t, make_sdesc(sf_addr, 0, 128, kLayoutNone));
+#pragma unroll
+            for (int b = 0; b < C::BN / 128; ++b)
+              ptx::tc_cp_32x128b_x4(sfb_t + 4u * b,
+                                    make_sdesc(sf_addr + C::SFA_BYTES + 512 * b, 0, 128, kLayoutNone));
+#pragma unroll
+            for (int kk = 0; kk < C::K_STEPS; ++kk) {
+              const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
+              const uint64_t bd =
+                  make_sdesc(b_addr + kk * C::MMA_K * 128, C::B_ATOM_BYTES, 1024, kLayoutSW128);
+              const uint32_t idesc = C::IDESC_MXF8 | (uint32_t(kk) << 4) | (uint32_t(kk) << 29);
+              ptx::mma_mxf8(d_tmem, ad, bd, idesc, sfa_t, sfb_t,
+                            (kb != uc.kb_begin || kk != 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < C::K_STEPS; ++kk) {
+              const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
+              const uint64_t bd =
+                  make_sdesc(b_addr + kk * C::MMA_K * 128, C::B_ATOM_BYTES, 1024, kLayoutSW128);
+              ptx::mma_bf16(d_tmem, ad, bd, C::IDESC_BF16, (kb != uc.kb_begin || kk != 0) ? 1u : 0u);
+            }
+          }
+          issued_any = true;
+          ptx::tc_commit(empty_bar(stage));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit(tfull_bar(buf));
+        if (++buf == C::ACC_BUFS) {
+          buf = 0;
+          bphase ^= 1u;
+        }
+      }
+      if (!ok && issued_any) {
+        // wait for the MMAs already issued before TMEM is released
+        ptx::tc_commit(drain_bar);
+        SyncCtx drain{abort_flag, p.status, p.timeout_ns};
+        volatile uint32_t no_abort = 0;
+        drain.abort = &no_abort;
+        wait_phase(drain_bar, 0u, drain, kErrTimeoutMma);
+      }
+    }
+    __syncwarp();
+  } else if (C::kFp8 && warp == 2) {
+    // ------------------------------------------------------------ scale producer (MXFP8)
+    // Layout expected by tcgen05.cp 32x128b.warpx4 for 128 rows x 4 k-blocks (512 bytes):
+    // byte (r % 32) * 16 + (r / 32) * 4 + kblk.  One 512-byte block for x's rows, one per
+    // 128 columns of W.
+    int stage = 0;
+    uint32_t phase = 0;
+    const int KB32 = p.K / 32;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const UnitCoord uc = unit_coord(u, p);
+      for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
+        if (!warp_wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutScales)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sf_addr = sbase + C::OFF_SF + stage * C::SF_BYTES;
+        uint32_t wa[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int row = uc.m_tile * kBM + g * 32 + lane;
+          wa[g] = row < p.M ? __ldg(reinterpret_cast<const uint32_t*>(p.sx + (size_t)row * KB32) + kb)
+                            : 0x7F7F7F7Fu;
+        }
+        ptx::st_shared_v4(sf_addr + lane * 16, wa[0], wa[1], wa[2], wa[3]);
+#pragma unroll
+        for (int b = 0; b < C::BN / 128; ++b) {
+          uint32_t wb[4];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int col = uc.n_tile * C::BN + b * 128 + g * 32 + lane;
+            uint32_t v = 0x7F7F7F7Fu;
+            if (col < p.N) {
+              v = 0;
+#pragma unroll
+              for (int t = 0; t < 4; ++t)
+                v |= uint32_t(__ldg(p.sw + (size_t)(kb * 4 + t) * p.N + col)) << (8 * t);
+            }
+            wb[g] = v;
+          }
+          ptx::st_shared_v4(sf_addr + C::SFA_BYTES + b * 512 + lane * 16, wb[0], wb[1], wb[2], wb[3]);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(full_bar(stage));
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= C::EPI_WARP0) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int epi_tid = (warp - C::EPI_WARP0) * 32 + lane;
+    int buf = 0;
+    uint32_t bphase = 0, ephase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const UnitCoord uc = unit_coord(u, p);
+      if (!warp_wait_phase(tfull_bar(buf), bphase, sc, kErrTimeoutEpilogue)) break;
+      ptx::tc_fence_after();
+      const int row_in_tile = q * 32 + lane;
+      const int row = uc.m_tile * kBM + row_in_tile;
+      const int col_tile0 = uc.n_tile * C::BN;
+#pragma unroll 1
+      for (int c = 0; c < C::BN / 32; ++c) {
+        const int col0 = col_tile0 + c * 32;
+        if (col0 >= p.N) break;             // uniform across the warp
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(tmem_base + uint32_t(buf * C::BN + c * 32) + (uint32_t(q * 32) << 16), r);
+        ptx::tmem_wait_ld();
+        const int nvalid = min(32, p.N - col0);
+        if (row < p.M) {
+          if (p.splits > 1) {
+            float* dst = p.ws + ((((size_t)uc.tile * p.splits + uc.s) * kBM + row_in_tile) * C::BN + c * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              if (v * 4 < nvalid) ptx::st_global_v4(dst + v * 4, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+          } else if constexpr (C::kOutF32) {
+            float* dst = reinterpret_cast<float*>(p.y) + (size_t)row * p.N + col0;
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              if (v * 4 < nvalid) ptx::st_global_v4(dst + v * 4, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+          } else {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)row * p.N + col0;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (v * 8 < nvalid) {
+                const float* f = reinterpret_cast<const float*>(r + 8 * v);
+                ptx::st_global_v4(dst + v * 8, ptx::pack_bf16x2(f[0], f[1]), ptx::pack_bf16x2(f[2], f[3]),
+                                  ptx::pack_bf16x2(f[4], f[5]), ptx::pack_bf16x2(f[6], f[7]));
+              }
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
+      if (++buf == C::ACC_BUFS) {
+        buf = 0;
+        bphase ^= 1u;
+      }
+      if (p.splits > 1) {
+        // Fixed-order merge of the S partials by the last CTA to arrive at this tile.
+        // Hand-off 1: every partial of this CTA is stored and fenced before the count.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(epi_bar);
+        if (!warp_wait_phase(epi_bar, ephase, sc, kErrTimeoutEpilogue)) break;
+        ephase ^= 1u;
+        if (epi_tid == 0) {
+          const uint32_t old = atomicAdd(p.counters + uc.tile, 1u);
+          *last_flag = (old == uint32_t(p.splits - 1)) ? 1u : 0u;
+        }
+        // Hand-off 2: the verdict is visible to all four warps.
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(epi_bar);
+        if (!warp_wait_phase(epi_bar, ephase, sc, kErrTimeoutEpilogue)) break;
+        ephase ^= 1u;
+        const bool last = *last_flag != 0u;
+        if (last) {
+          __threadfence();
+          if (row < p.M) {
+            const float* src0 = p.ws + (((size_t)uc.tile * p.splits) * kBM + row_in_tile) * C::BN;
+            const size_t sstride = (size_t)kBM * C::BN;
+#pragma unroll 1
+            for (int c = 0; c < C::BN / 32; ++c) {
+              const int col0 = col_tile0 + c * 32;
+              if (col0 >= p.N) break;
+              const int nvalid = min(32, p.N - col0);
+#pragma unroll 1
+              for (int v = 0; v < 8; ++v) {
+                if (v * 4 >= nvalid) break;
+                const float* sp = src0 + c * 32 + v * 4;
+                float4 acc = __ldcg(reinterpret_cast<const float4*>(sp));
+#pragma unroll 1
+                for (int s = 1; s < p.splits; ++s) {
+                  const float4 t = __ldcg(reinterpret_cast<const float4*>(sp + s * sstride));
+                  acc.x = acc.x + t.x;
+                  acc.y = acc.y + t.y;
+                  acc.z = acc.z + t.z;
+                  acc.w = acc.w + t.w;
+                }
+                if constexpr (C::kOutF32) {
+                  float* dst = reinterpret_cast<float*>(p.y) + (size_t)row * p.N + col0 + v * 4;
+                  *reinterpret_cast<float4*>(dst) = acc;
+                } else {
+                  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)row * p.N + col0 + v * 4;
+                  uint2 pk;
+                  pk.x = ptx::pack_bf16x2(acc.x, acc.y);
+                  pk.y = ptx::pack_bf16x2(acc.z, acc.w);
+                  *reinterpret_cast<uint2*>(dst) = pk;
+                }
+              }
+            }
+          }
+          if (epi_tid == 0) p.counters[uc.tile] = 0u;   // ready for the next launch
+        }
+        // Hand-off 3: last_flag may be rewritten only after every warp has read it.
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(epi_bar);
+        if (!warp_wait_phase(epi_bar, ephase, sc, kErrTimeoutEpilogue)) break;
+        ephase ^= 1u;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace bigemm

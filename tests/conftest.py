@@ -10,6 +10,14 @@ if ROOT not in sys.path:
 GOLDEN = os.path.join(ROOT, "tests", "golden")
 
 
+def pytest_sessionstart(session):
+    """Build the oracle (gcc) and the CUDA libraries (nvcc, sm_103a) if they are stale."""
+    import oracle.build
+    import invariant_bi_gemm_gb300.build
+    oracle.build.build()
+    invariant_bi_gemm_gb300.build.build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: takes more than a few seconds")

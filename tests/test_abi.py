@@ -1,0 +1,96 @@
+"""Host-side checks of the C ABI that need no GPU: the libraries load, export every symbol
+the headers declare, and refuse bad arguments with the documented codes before any CUDA
+call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import invariant_bi_gemm_gb300 as bg
+from invariant_bi_gemm_gb300 import build as bgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared(header):
+    src = open(os.path.join(ROOT, "include", header)).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(bi_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_symbols_exported():
+    declared = _declared("bi_gemm.h")
+    assert set(declared) == set(bg.EXPORTED_SYMBOLS)
+    L = ctypes.CDLL(bgbuild.lib_path("libbi_gemm.so"))
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_controls_symbols_exported():
+    declared = _declared("bi_gemm_controls.h")
+    assert declared, "controls header declares nothing"
+    L = ctypes.CDLL(bgbuild.lib_path("libbi_gemm_controls.so"))
+    for name in declared:
+        assert hasattr(L, name), name
+    # the control library hides its private copy of the product ABI
+    assert not hasattr(L, "bi_gemm_run")
+
+
+def test_version_and_strerror():
+    assert bg.bi_gemm_version() >> 16 == 1
+    for code in range(0, -7, -1):
+        assert bg.bi_gemm_strerror(code) and "unknown" not in bg.bi_gemm_strerror(code)
+    assert "unknown" in bg.bi_gemm_strerror(-99)
+
+
+@pytest.mark.parametrize("K,N,dtype,layout,want", [
+    (256, 128, 7, 0, bg.BI_GEMM_ERR_INVALID_ARG),        # bad dtype
+    (256, 128, 0, 5, bg.BI_GEMM_ERR_INVALID_ARG),        # bad scale layout
+    (-1, 128, 0, 0, bg.BI_GEMM_ERR_INVALID_ARG),
+    (0, 128, 0, 0, bg.BI_GEMM_ERR_UNSUPPORTED),
+    (250, 128, 0, 0, bg.BI_GEMM_ERR_UNSUPPORTED),        # bf16 row pitch not 16 B
+    (256, 100, 1, 0, bg.BI_GEMM_ERR_UNSUPPORTED),
+    (256, 128, 0, 1, bg.BI_GEMM_ERR_UNSUPPORTED),        # bf16 with scales
+    (192, 128, 2, 1, bg.BI_GEMM_ERR_UNSUPPORTED),        # MXFP8 K % 128
+    (256, 120, 2, 1, bg.BI_GEMM_ERR_UNSUPPORTED),        # MXFP8 N % 16
+    (256, 128, 2, 0, bg.BI_GEMM_ERR_UNSUPPORTED),        # MXFP8 without scales
+])
+def test_create_refuses_before_touching_cuda(K, N, dtype, layout, want):
+    h = ctypes.c_void_p()
+    rc = bg.library().bi_gemm_create(ctypes.byref(h), K, N, dtype, layout)
+    assert rc == want
+    assert h.value is None
+
+
+def test_null_arguments():
+    L = bg.library()
+    assert L.bi_gemm_create(None, 256, 128, 0, 0) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_gemm_run(None, None, 4, None, None, None, None) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_gemm_get_device_error(None, None) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_gemm_destroy(None) == bg.BI_GEMM_OK
+    assert L.bi_gemm_get_config(None, None) == bg.BI_GEMM_ERR_INVALID_ARG
+    b = ctypes.c_uint64()
+    assert L.bi_gemm_workspace_size(None, 4, ctypes.byref(b)) == bg.BI_GEMM_ERR_INVALID_ARG
+    opts = bg.bi_gemm_options(-1, 0, 0)
+    h = ctypes.c_void_p()
+    assert L.bi_gemm_create_ex(ctypes.byref(h), 256, 128, 0, 0, ctypes.byref(opts)) == bg.BI_GEMM_ERR_INVALID_ARG
+    opts = bg.bi_gemm_options(5, 0, 0)   # 5 > ceil(256 / 64) k-blocks
+    assert L.bi_gemm_create_ex(ctypes.byref(h), 256, 128, 0, 0, ctypes.byref(opts)) == bg.BI_GEMM_ERR_INVALID_ARG
+
+
+def test_product_binding_has_no_fallback(monkeypatch, tmp_path):
+    """Without the built library the binding raises instead of computing anything."""
+    monkeypatch.setattr(bgbuild, "lib_path", lambda name="libbi_gemm.so": str(tmp_path / name))
+    monkeypatch.setattr(bg, "_lib", None)
+    with pytest.raises(ImportError):
+        bg.library()
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "invariant_bi_gemm_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "bi_oracle" not in src and "from oracle" not in src and "import oracle" not in src

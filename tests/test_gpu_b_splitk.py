@@ -1,0 +1,66 @@
+"""Small-N long-K GEMM, the split-K-tempting shape of "[BI][DSv4] Make mHC tilelang ops batch
+invariant": fp32 out of bf16 x[M,16384]·W[16384,24], rows of x scaled by 2.08 / 0.019 / 0.245
+in turn (the page's checkpoint-realistic magnitudes), W~N(0,0.02), M = 1..256 every value.
+The handle pins the split count to 32 with an ordered serial merge; every row must be
+bitwise the same at every M, and within 1e-5 * S_abs of the oracle."""
+import numpy as np
+import pytest
+
+import inputgen as ig
+import oracle
+from gpu_util import bi_check, check_tolerance, dev_bf16, host_bits
+from invariant_bi_gemm_gb300 import BiGemm
+
+pytestmark = pytest.mark.gpu
+
+K, N, MMAX = 16384, 24, 256
+
+
+@pytest.fixture(scope="module")
+def setup():
+    W = ig.normal_bf16(ig.SEED_W, K, N, std=0.02)
+    X = ig.scaled_rows_bf16(ig.SEED_X, MMAX, K)
+    g = BiGemm(K, N, "bf16_f32")
+    y_ref, _, sabs = oracle.gemm_bf16(X, W, "f32")
+    yield g, dev_bf16(W), dev_bf16(X), y_ref, sabs
+    g.close()
+
+
+def test_split_is_pinned(setup):
+    c = setup[0].config
+    assert c["split_k"] == 32 and c["block_n"] == 64
+
+
+def test_parity_and_rows_identical_for_every_m(setup):
+    g, Wd, Xd, y_ref, sabs = setup
+    y_full = host_bits(g(Xd, Wd))
+    worst = check_tolerance(y_full, y_ref, sabs, oracle.TOL_F32, "M=256")
+    for M in range(1, MMAX + 1):
+        yM = host_bits(g(Xd[:M].contiguous(), Wd))
+        assert np.array_equal(yM.view(np.uint32), y_full[:M].view(np.uint32)), f"M={M}"
+    assert g.device_error() == 0
+    print(f"split-K fp32 max |y-y_ref|/S_abs = {worst:.3g}")
+
+
+def test_bi_cells_across_batch_boundaries(setup):
+    g, Wd, Xd, _, _ = setup
+    C = dev_bf16(ig.scaled_rows_bf16(ig.SEED_C, 1, K))[0]
+    A = dev_bf16(ig.scaled_rows_bf16(ig.SEED_A, MMAX, K))
+    B = dev_bf16(ig.scaled_rows_bf16(ig.SEED_B, MMAX, K))
+    golden = host_bits(g(C[None].contiguous(), Wd))
+    total = 0
+    for M in (1, 7, 8, 15, 16, 17, 63, 64, 65, 127, 128, 129, 192, 193, 255, 256):
+        for t, d_ab, d_g in bi_check(lambda x: g(x, Wd), A, B, C, M, golden):
+            total += d_ab + d_g
+    assert total == 0
+
+
+def test_forced_split_counts_agree_with_oracle(setup):
+    """Any fixed split count is a valid configuration; each stays within tolerance."""
+    _, Wd, Xd, y_ref, sabs = setup
+    for s in (1, 2, 8, 64, 256):
+        g = BiGemm(K, N, "bf16_f32", split_k=s)
+        assert g.config["split_k"] == s
+        y = host_bits(g(Xd[:130].contiguous(), Wd))
+        check_tolerance(y, y_ref[:130], sabs[:130], oracle.TOL_F32, f"S={s}")
+        g.close()

@@ -1,0 +1,91 @@
+"""LLM projection sweep: bf16 x[M,4096]~N(0,1) · W[4096,14336]~N(0,0.02), bf16 out,
+M in {1,7,8,15,16,17,63,64,65,128,129,192,193,256} (the batch boundaries of "[BI][DSv4] Make
+mHC tilelang ops batch invariant", "Tests") extended to 512..8192.  Rows are compared
+bitwise across all M; sampled rows against the oracle; A/B cells at {0, mid, last}."""
+import numpy as np
+import pytest
+import torch
+
+import inputgen as ig
+import oracle
+from gpu_util import bi_check, check_tolerance, dev_bf16, host_bits
+from invariant_bi_gemm_gb300 import BiGemm
+
+pytestmark = pytest.mark.gpu
+
+K, N = 4096, 14336
+M_LIST = [1, 7, 8, 15, 16, 17, 63, 64, 65, 128, 129, 192, 193, 256, 512, 1024, 2048, 4096, 8192]
+MMAX = M_LIST[-1]
+
+
+def sample_rows():
+    rows = {0, 1, 6, 7, 8, 14, 15, 16, 62, 63, 64, 127, 128, 191, 192, 255, 511, 1023, 2047,
+            4095, 4096, 8191}
+    rng = np.random.default_rng(7)
+    rows |= set(int(r) for r in rng.integers(0, MMAX, 10))
+    return sorted(rows)
+
+
+@pytest.fixture(scope="module")
+def setup():
+    W = ig.normal_bf16(ig.SEED_W, K, N, std=0.02)
+    X = ig.normal_bf16(ig.SEED_X, MMAX, K)
+    g = BiGemm(K, N, "bf16")
+    Wd, Xd = dev_bf16(W), dev_bf16(X)
+    y_full = g(Xd, Wd)
+    yield g, W, X, Wd, Xd, y_full
+    g.close()
+
+
+def test_config(setup):
+    c = setup[0].config
+    assert (c["block_m"], c["block_n"], c["mma_n"], c["split_k"]) == (128, 256, 256, 1)
+
+
+def test_rows_bitwise_identical_across_m(setup):
+    g, W, X, Wd, Xd, y_full = setup
+    for M in M_LIST:
+        yM = g(Xd[:M], Wd)
+        assert torch.equal(yM.view(torch.int16), y_full[:M].view(torch.int16)), f"M={M}"
+    assert g.device_error() == 0
+
+
+def test_parity_sampled_rows(setup):
+    g, W, X, Wd, Xd, y_full = setup
+    rows = sample_rows()
+    y_ref, _, sabs = oracle.gemm_bf16(X, W, "bf16", rows=rows)
+    y = host_bits(y_full)[rows]
+    worst = check_tolerance(y, y_ref, sabs, oracle.TOL_BF16, "LLM projection")
+    # bf16 output: almost every element equals the exactly rounded value
+    agree = float(np.mean(y == y_ref))
+    print(f"LLM bf16 max ratio {worst:.3g}, bitwise agreement with oracle {agree:.4f}")
+    assert agree > 0.99
+
+
+def test_bi_cells(setup):
+    g, W, X, Wd, Xd, y_full = setup
+    C = dev_bf16(ig.normal_bf16(ig.SEED_C, 1, K))[0]
+    A = dev_bf16(ig.normal_bf16(ig.SEED_A, MMAX, K))
+    B = dev_bf16(ig.normal_bf16(ig.SEED_B, MMAX, K))
+    golden = host_bits(g(C[None].contiguous(), Wd))
+    total = 0
+    for M in M_LIST:
+        for t, d_ab, d_g in bi_check(lambda x: g(x, Wd), A, B, C, M, golden):
+            total += d_ab + d_g
+    assert total == 0
+
+
+def test_repeat_run_bitwise():
+    """Run-to-run determinism, the nondeterminism article's 2048x2048 bf16 example repeated
+    1000 times: every output is bitwise the first."""
+    A = dev_bf16(ig.normal_bf16(11, 2048, 2048))
+    Bm = dev_bf16(ig.normal_bf16(12, 2048, 2048))
+    g = BiGemm(2048, 2048, "bf16")
+    ref = g(A, Bm)
+    y = torch.empty_like(ref)
+    same = 0
+    for _ in range(1000):
+        g(A, Bm, y)
+        same += int(torch.equal(y.view(torch.int16), ref.view(torch.int16)))
+    assert same == 1000
+    g.close()
