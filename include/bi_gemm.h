@@ -70,8 +70,10 @@ enum {
   BI_GEMM_ERR_ALIGNMENT = -3,    /* a pointer or row pitch breaks the 16-byte rule          */
   BI_GEMM_ERR_CUDA = -4,         /* a CUDA runtime call failed (launch, allocation setup)   */
   BI_GEMM_ERR_OOM = -5,          /* workspace allocation failed                             */
-  BI_GEMM_ERR_TIMEOUT = -6       /* a bounded in-kernel wait expired (reported by
+  BI_GEMM_ERR_TIMEOUT = -6,      /* a bounded in-kernel wait expired (reported by
                                     bi_gemm_get_device_error)                               */
+  BI_GEMM_ERR_SCRATCH_LIMIT = -7 /* bi_gemm_run_noalloc: the run needs more scratch than its
+                                    fixed array holds                                       */
 };
 
 /* Create a handle for y = x·W with fixed K and N.  Selects and records the single kernel
@@ -105,6 +107,31 @@ int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtype, int scale
  * Errors from the kernel's bounded waits are reported by bi_gemm_get_device_error. */
 int bi_gemm_run(bi_gemm_t h, const void* x, int64_t M, const void* W,
                 const bi_gemm_scales* scales, void* y, void* stream);
+
+/* Allocation-free variant of bi_gemm_run (the papers have no counterpart; this is a service
+ * of this library).  It is for callers that may not allocate device memory when they run a
+ * GEMM: code whose device memory is wholly owned and budgeted by another framework's pool,
+ * latency-critical loops that must not enter the allocator (its locks and implicit
+ * synchronisation), and code running where CUDA allocation calls are not permitted.
+ * Same arguments, layouts, kernel and results as bi_gemm_run on the same handle; the
+ * difference is where a split count S > 1 keeps its scratch (one uint32 arrival counter per
+ * output tile and tiles*S*128*BN fp32 partials): instead of the handle's workspace, grown with
+ * cudaMallocAsync, it uses one fixed 8 MiB device array compiled into the library (4 KiB of
+ * counters, so at most 1024 output tiles, then 8 MiB - 4 KiB of partials).  Every GPU on which
+ * the library's kernels are loaded holds that array until the process exits.  This call makes
+ * no cudaMalloc, cudaMallocAsync or cudaFree and calls no allocating library routine.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current) and remembers it; make that first call before any stream
+ *     capture.  The handle's device must be current (else BI_GEMM_ERR_INVALID_ARG).
+ *   - A run whose scratch would not fit returns BI_GEMM_ERR_SCRATCH_LIMIT and queues nothing:
+ *     tiles = ceil(M/128) * ceil(N/BN) must be <= 1024 and tiles*S*128*BN*4 bytes must be
+ *     <= 8 MiB - 4 KiB (bi_gemm_get_config gives S and BN).  Handles with S == 1 use no scratch.
+ *   - All calls in the process share the one array per device and it keeps the last call's
+ *     contents; each call first clears, on `stream`, the counters it uses.  Calls whose work
+ *     overlaps on the GPU (other streams, other threads, other handles) race on the array and
+ *     give undefined results: serialise them. */
+int bi_gemm_run_noalloc(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                        const bi_gemm_scales* scales, void* y, void* stream);
 
 /* Synchronise `stream`, then read and clear the handle's device status word: BI_GEMM_OK,
  * or BI_GEMM_ERR_TIMEOUT if any run since the last call had a bounded wait expire (its

@@ -29,12 +29,13 @@ BI_GEMM_ERR_ALIGNMENT = -3
 BI_GEMM_ERR_CUDA = -4
 BI_GEMM_ERR_OOM = -5
 BI_GEMM_ERR_TIMEOUT = -6
+BI_GEMM_ERR_SCRATCH_LIMIT = -7
 
 # every symbol include/bi_gemm.h declares
 EXPORTED_SYMBOLS = (
     "bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_get_device_error",
     "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_strerror",
-    "bi_gemm_version",
+    "bi_gemm_version", "bi_gemm_run_noalloc",
 )
 
 
@@ -69,6 +70,7 @@ def _load() -> ctypes.CDLL:
     L.bi_gemm_create.argtypes = [ctypes.POINTER(P), I64, I64, I32, I32]
     L.bi_gemm_create_ex.argtypes = [ctypes.POINTER(P), I64, I64, I32, I32, ctypes.POINTER(bi_gemm_options)]
     L.bi_gemm_run.argtypes = [P, P, I64, P, ctypes.POINTER(bi_gemm_scales), P, P]
+    L.bi_gemm_run_noalloc.argtypes = [P, P, I64, P, ctypes.POINTER(bi_gemm_scales), P, P]
     L.bi_gemm_get_device_error.argtypes = [P, P]
     L.bi_gemm_destroy.argtypes = [P]
     L.bi_gemm_get_config.argtypes = [P, ctypes.POINTER(bi_gemm_config)]
@@ -76,7 +78,7 @@ def _load() -> ctypes.CDLL:
     L.bi_gemm_strerror.argtypes = [I32]
     L.bi_gemm_strerror.restype = ctypes.c_char_p
     L.bi_gemm_version.argtypes = []
-    for n in ("bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_get_device_error",
+    for n in ("bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_run_noalloc", "bi_gemm_get_device_error",
               "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_version"):
         getattr(L, n).restype = I32
     return L
@@ -128,6 +130,17 @@ def bi_gemm_run(h: int, x: int, M: int, W: int, scales: bi_gemm_scales | None, y
                          ctypes.byref(scales) if scales is not None else None, ctypes.c_void_p(y),
                          ctypes.c_void_p(stream))
     _check(rc, "bi_gemm_run")
+
+
+def bi_gemm_run_noalloc(h: int, x: int, M: int, W: int, scales: bi_gemm_scales | None, y: int,
+                        stream: int) -> None:
+    """bi_gemm_run for callers that may not allocate device memory: a split count > 1 keeps its
+    scratch in the library's fixed 8 MiB per-device array; too large a run raises
+    BiGemmError(BI_GEMM_ERR_SCRATCH_LIMIT).  Calls that overlap on the GPU race on that array."""
+    rc = library().bi_gemm_run_noalloc(ctypes.c_void_p(h), ctypes.c_void_p(x), int(M), ctypes.c_void_p(W),
+                                       ctypes.byref(scales) if scales is not None else None, ctypes.c_void_p(y),
+                                       ctypes.c_void_p(stream))
+    _check(rc, "bi_gemm_run_noalloc")
 
 
 def bi_gemm_get_device_error(h: int, stream: int = 0) -> int:
@@ -235,7 +248,7 @@ class BiGemm:
 
 
 __all__ = [
-    "BiGemm", "BiGemmError", "bi_gemm_create", "bi_gemm_run", "bi_gemm_get_device_error",
+    "BiGemm", "BiGemmError", "bi_gemm_create", "bi_gemm_run", "bi_gemm_run_noalloc", "bi_gemm_get_device_error",
     "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_strerror",
     "bi_gemm_version", "bi_gemm_scales", "bi_gemm_options", "EXPORTED_SYMBOLS", "LIB_PATH", "library",
 ]

@@ -414,8 +414,126 @@ BI_GEMM_API const char* bi_gemm_strerror(int code) {
     case BI_GEMM_ERR_CUDA: return "CUDA runtime error";
     case BI_GEMM_ERR_OOM: return "workspace allocation failed";
     case BI_GEMM_ERR_TIMEOUT: return "bounded in-kernel wait expired";
+    case BI_GEMM_ERR_SCRATCH_LIMIT: return "problem too large for the fixed scratch of bi_gemm_run_noalloc";
     default: return "unknown error code";
   }
 }
 
 BI_GEMM_API int bi_gemm_version(void) { return kVersion; }
+
+#ifndef BI_GEMM_CONTROLS
+// ------------------------------------------------------------------ allocation-free run
+//
+// bi_gemm_run grows a per-handle workspace with cudaMallocAsync when a split count S > 1 needs
+// fp32 partials.  Some callers may not allocate device memory at call time: code whose device
+// memory is entirely owned and budgeted by another framework's pool (a raw allocation there can
+// fail or fragment it), latency-critical loops that must not take the allocator's locks or its
+// implicit synchronisation, and code running where CUDA API allocation is not permitted.
+// bi_gemm_run_noalloc gives them the same split-K kernel with its scratch (arrival counters and
+// partials) in one fixed device array below, compiled into the library.
+//
+// The array is kNoAllocScratchBytes per device; every GPU on which this library's kernels are
+// loaded holds it until the process exits.  Host code may not use the array's name as a device
+// address (it is a host-side stand-in); the device address is fetched once per device with
+// cudaGetSymbolAddress, with that device current, on the first bi_gemm_run_noalloc call there.
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;     // 8 MiB per device
+constexpr size_t kNoAllocCounterBytes = 4096;                // arrival counters, <= 1024 tiles
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+int noalloc_scratch_address(int dev, char** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return BI_GEMM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return BI_GEMM_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = static_cast<char*>(g_noalloc_ptr[dev]);
+  return BI_GEMM_OK;
+}
+
+}  // namespace
+
+BI_GEMM_API int bi_gemm_run_noalloc(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                                    const bi_gemm_scales* scales, void* y, void* stream) {
+  int rc = validate_run(h, x, M, W, scales, y);
+  if (rc != BI_GEMM_OK || M == 0) return rc;
+  std::lock_guard<std::mutex> lk(h->mu);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return BI_GEMM_ERR_CUDA;
+  }
+  if (dev != h->device) return BI_GEMM_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool fp8 = h->dtype == BI_MXFP8E4M3_OUT_BF16;
+  const int split = h->split;
+  const int64_t m_tiles = (M + kBM - 1) / kBM;
+  const int64_t tiles = m_tiles * h->n_tiles;
+  if (tiles * split >= (int64_t(1) << 31)) return BI_GEMM_ERR_UNSUPPORTED;
+  char* scratch = nullptr;
+  if (split > 1) {
+    const size_t part = size_t(tiles) * split * kBM * h->kern.bn * sizeof(float);
+    if (size_t(tiles) * sizeof(uint32_t) > kNoAllocCounterBytes ||
+        part > kNoAllocScratchBytes - kNoAllocCounterBytes)
+      return BI_GEMM_ERR_SCRATCH_LIMIT;
+    rc = noalloc_scratch_address(dev, &scratch);
+    if (rc != BI_GEMM_OK) return rc;
+  }
+
+  CUtensorMap tmap_x;
+  if (!encode_2d(&tmap_x, x, fp8, uint64_t(M), uint64_t(h->K), kBM, 128 / (fp8 ? 1 : 2)))
+    return BI_GEMM_ERR_CUDA;
+  if (h->w_cached != W) {
+    if (!encode_2d(&h->tmap_w, W, fp8, uint64_t(h->K), uint64_t(h->N), h->kern.bk,
+                   128 / (fp8 ? 1 : 2))) {
+      h->w_cached = nullptr;
+      return BI_GEMM_ERR_CUDA;
+    }
+    h->w_cached = W;
+  }
+  // The previous call's counters are normally back at zero, but an aborted run can leave them
+  // set: clear the ones this call uses.  Partials need no clearing (written before read).
+  if (split > 1 && cudaMemsetAsync(scratch, 0, size_t(tiles) * sizeof(uint32_t), st) != cudaSuccess) {
+    cudaGetLastError();
+    return BI_GEMM_ERR_CUDA;
+  }
+
+  KParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.y = y;
+  p.sx = scales ? scales->sx : nullptr;
+  p.sw = scales ? scales->sw : nullptr;
+  p.counters = split > 1 ? reinterpret_cast<uint32_t*>(scratch) : nullptr;
+  p.ws = split > 1 ? reinterpret_cast<float*>(scratch + kNoAllocCounterBytes) : nullptr;
+  p.status = h->d_status;
+  p.M = int32_t(M);
+  p.N = int32_t(h->N);
+  p.K = int32_t(h->K);
+  p.m_tiles = int32_t(m_tiles);
+  p.n_tiles = int32_t(h->n_tiles);
+  p.splits = split;
+  p.kblocks = h->kblocks;
+  p.timeout_ns = h->timeout_ns;
+  p.test_flags = 0u;
+  const int grid = int(std::min<int64_t>(tiles * split, h->max_ctas));
+  void* args[3] = {&tmap_x, &h->tmap_w, &p};
+  if (cudaLaunchKernel(h->kern.fn, dim3(grid), dim3(h->kern.threads), args, size_t(h->kern.smem), st) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return BI_GEMM_ERR_CUDA;
+  }
+  return BI_GEMM_OK;
+}
+#endif
