@@ -92,6 +92,10 @@ typedef struct {
                              count (1 <= split_k <= ceil(K / BK)); still never M-dependent */
   int32_t max_ctas;       /* 0 = one CTA per SM; otherwise an upper bound on the grid     */
   uint64_t timeout_ns;    /* 0 = default (5 s); limit of every in-kernel wait             */
+  int32_t prefetch_kb;    /* L2 prefetch distance of W in K stages: 0 or -1 = none (the
+                             default), 1..1024 = request W this many stages ahead of the
+                             shared-memory ring.  A memory hint only: results are bitwise
+                             the same for every setting.                                  */
 } bi_gemm_options;
 
 /* bi_gemm_create with explicit options (NULL = defaults, same as bi_gemm_create). */
@@ -144,7 +148,8 @@ int bi_gemm_destroy(bi_gemm_t h);
 
 /* The fixed configuration recorded in a handle. */
 typedef struct {
-  int32_t block_m, block_n, block_k;  /* output tile rows / columns, K per pipeline stage  */
+  int32_t block_m, block_n, block_k;  /* output tile rows / columns, K per pipeline stage
+                                         (a CTA pair's tile is 256 x 256)                   */
   int32_t mma_m, mma_n, mma_k;        /* tcgen05.mma instruction shape                     */
   int32_t stages;                     /* shared-memory pipeline depth                       */
   int32_t split_k;                    /* S: fixed K split count (1 = none)                  */
@@ -153,6 +158,8 @@ typedef struct {
   int32_t threads;                    /* threads per CTA                                    */
   int32_t smem_bytes;                 /* dynamic shared memory per CTA                      */
   int32_t tmem_cols;                  /* tensor-memory columns per CTA                      */
+  int32_t ctas_per_tile;              /* 1, or 2 for a CTA-pair tile (tcgen05 cta_group::2) */
+  int32_t max_groups;                 /* resident CTA groups (CTAs or pairs) in the grid    */
 } bi_gemm_config;
 
 int bi_gemm_get_config(bi_gemm_t h, bi_gemm_config* cfg);

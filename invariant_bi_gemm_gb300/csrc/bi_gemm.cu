@@ -4,8 +4,9 @@
 // The configuration rule ("Batch-invariant matrix multiplication", nondeterminism article:
 // compile one kernel configuration and use it for all shapes; strategy switches keyed on
 // the block/SM ratio are where libraries lose invariance):
-//   tile      128 x BN, BN = 64 / 128 / 256 (bf16) or 128 / 256 (MXFP8) from N alone;
-//   MMA       tcgen05.mma M=128, N=BN, K=16 (bf16) or K=32 (MXFP8 block-scaled);
+//   tile      128 x BN, BN = 64 / 128 / 256 (bf16) or 128 / 256 (MXFP8) from N alone; for
+//             bf16 with BN = 256 the tile is 256 x 256 on a CTA pair (cta_group::2);
+//   MMA       tcgen05.mma M=128 (M=256 on a pair), N=BN, K=16 (bf16) or K=32 (MXFP8);
 //   K stage   128 bytes of K per stage (64 bf16 / 128 E4M3), ascending k-blocks;
 //   split S   1, except for a single N tile (N <= BN) with a long K, where
 //             S = min(32, pow2floor(SMs / 4), pow2floor(KB / 8)) — the pinned
@@ -38,7 +39,8 @@ constexpr uint64_t kDefaultTimeoutNs = 5ull * 1000 * 1000 * 1000;
 
 struct KernelInfo {
   const void* fn = nullptr;
-  int threads = 0, smem = 0, tmem_cols = 0, stages = 0, bn = 0, bk = 0, mma_k = 0;
+  int threads = 0, smem = 0, tmem_cols = 0, stages = 0, bn = 0, bk = 0, mma_k = 0, ctas = 1;
+  int w_box_cols = 0, w_swizzle = 128;   // TMA box width of W (columns) and its swizzle span
 };
 
 template <class C>
@@ -52,8 +54,16 @@ KernelInfo info_of() {
   k.bn = C::BN;
   k.bk = C::BK;
   k.mma_k = C::MMA_K;
+  k.ctas = C::CTAS;
+  k.w_box_cols = C::ATOM_N;
+  k.w_swizzle = C::B_SW;
   return k;
 }
+
+// Pipeline depth of the CTA-pair tile (a stage: 16 KB of x and 16 KB of W per CTA).
+#ifndef BI_GEMM_PAIR_STAGES
+#define BI_GEMM_PAIR_STAGES 6
+#endif
 
 // dtype 0/1: bf16 in, bf16/f32 out; dtype 2: MXFP8 in, bf16 out.
 static KernelInfo select_kernel(int dtype, int bn) {
@@ -61,11 +71,11 @@ static KernelInfo select_kernel(int dtype, int bn) {
     case BI_BF16_OUT_BF16:
       if (bn == 64) return info_of<KCfg<false, false, 64, 8, 2>>();
       if (bn == 128) return info_of<KCfg<false, false, 128, 6, 2>>();
-      return info_of<KCfg<false, false, 256, 4, 2>>();
+      return info_of<KCfg<false, false, 256, BI_GEMM_PAIR_STAGES, 2, 2>>();
     case BI_BF16_OUT_F32:
       if (bn == 64) return info_of<KCfg<false, true, 64, 8, 2>>();
       if (bn == 128) return info_of<KCfg<false, true, 128, 6, 2>>();
-      return info_of<KCfg<false, true, 256, 4, 2>>();
+      return info_of<KCfg<false, true, 256, BI_GEMM_PAIR_STAGES, 2, 2>>();
     default:
       if (bn == 128) return info_of<KCfg<true, false, 128, 6, 2>>();
       return info_of<KCfg<true, false, 256, 4, 1>>();
@@ -94,9 +104,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D row-major [rows, cols] tensor, box [box_rows, box_cols], 128-byte swizzle, zero fill.
+// 2-D row-major [rows, cols] tensor, box [box_rows, box_cols], 128- or 64-byte swizzle, zero fill.
 static bool encode_2d(CUtensorMap* m, const void* base, bool u8, uint64_t rows, uint64_t cols,
-                      uint32_t box_rows, uint32_t box_cols) {
+                      uint32_t box_rows, uint32_t box_cols, int swizzle = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   const uint64_t elem = u8 ? 1 : 2;
@@ -106,7 +116,8 @@ static bool encode_2d(CUtensorMap* m, const void* base, bool u8, uint64_t rows, 
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                   const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -120,6 +131,8 @@ struct bi_gemm {
   int dtype = 0, scale_layout = 0;
   int device = 0, num_sms = 0, max_ctas = 0;
   int split = 1, kblocks = 0, n_tiles = 0;
+  int max_groups = 0;      // CTA groups (single CTAs or pairs) resident at once
+  int prefetch_kb = -1;    // < 0: automatic
   uint64_t timeout_ns = kDefaultTimeoutNs;
   KernelInfo kern;
   uint32_t* d_status = nullptr;
@@ -155,7 +168,10 @@ int check_shape(int64_t K, int64_t N, int dtype, int scale_layout) {
   return BI_GEMM_OK;
 }
 
-int block_n_for(int64_t N, int dtype) {
+// Tile width from N alone: 64 / 128 for narrow N, else 256 (on a CTA pair for bf16).  (A
+// 192-wide pair tile, which would fill all 76 pairs at N = 14336, was measured slower at every
+// M on GB300: its 96-column W halves need 64-byte swizzle rows.)
+int block_n_for(int64_t N, int dtype, int /*num_sms*/) {
   if (dtype == BI_MXFP8E4M3_OUT_BF16) return N <= 128 ? 128 : 256;
   return N <= 64 ? 64 : (N <= 128 ? 128 : 256);
 }
@@ -205,59 +221,106 @@ int ensure_workspace(bi_gemm* h, int64_t tiles, int split, cudaStream_t st) {
   return BI_GEMM_OK;
 }
 
-// Launch one run; `split_override` > 0 replaces the handle's split count (control build only).
-int launch(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_gemm_scales* scales,
-           void* y, cudaStream_t st, int split_override, uint32_t test_flags) {
-  const bool fp8 = h->dtype == BI_MXFP8E4M3_OUT_BF16;
-  const int split = split_override > 0 ? split_override : h->split;
-  const int64_t m_tiles = (M + kBM - 1) / kBM;
-  const int64_t tiles = m_tiles * h->n_tiles;
-  if (tiles * split >= (int64_t(1) << 31)) return BI_GEMM_ERR_UNSUPPORTED;
+struct Shape {
+  int64_t m_tiles, tiles, subtiles;   // output tiles of TILE_M rows; 128-row sub-tiles
+};
 
+Shape shape_of(const bi_gemm* h, int64_t M) {
+  Shape sh;
+  const int64_t tile_m = int64_t(kBM) * h->kern.ctas;
+  sh.m_tiles = (M + tile_m - 1) / tile_m;
+  sh.tiles = sh.m_tiles * h->n_tiles;
+  sh.subtiles = sh.tiles * h->kern.ctas;
+  return sh;
+}
+
+// Encode the tensor maps, fill the kernel parameters and launch.  `ws` / `counters` are the
+// split-K scratch (ignored when split == 1).
+int launch_core(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_gemm_scales* scales,
+                void* y, cudaStream_t st, int split, float* ws, uint32_t* counters,
+                uint32_t test_flags) {
+  const bool fp8 = h->dtype == BI_MXFP8E4M3_OUT_BF16;
+  const Shape sh = shape_of(h, M);
+  if (sh.tiles * split >= (int64_t(1) << 31)) return BI_GEMM_ERR_UNSUPPORTED;
+
+  // x box: 128 rows, or only round_up(M, 8) rows when M < 128 (rows past M are never stored)
+  const uint32_t a_box_rows = M >= kBM ? uint32_t(kBM) : uint32_t((M + 7) / 8 * 8);
   CUtensorMap tmap_x;
-  if (!encode_2d(&tmap_x, x, fp8, uint64_t(M), uint64_t(h->K), kBM, 128 / (fp8 ? 1 : 2)))
+  if (!encode_2d(&tmap_x, x, fp8, uint64_t(M), uint64_t(h->K), a_box_rows, 128 / (fp8 ? 1 : 2)))
     return BI_GEMM_ERR_CUDA;
   if (h->w_cached != W) {
     if (!encode_2d(&h->tmap_w, W, fp8, uint64_t(h->K), uint64_t(h->N), h->kern.bk,
-                   128 / (fp8 ? 1 : 2))) {
+                   uint32_t(h->kern.w_box_cols), h->kern.w_swizzle)) {
       h->w_cached = nullptr;
       return BI_GEMM_ERR_CUDA;
     }
     h->w_cached = W;
   }
 
-  int rc = ensure_workspace(h, tiles, split, st);
-  if (rc != BI_GEMM_OK) return rc;
-
   KParams p;
   std::memset(&p, 0, sizeof(p));
   p.y = y;
   p.sx = scales ? scales->sx : nullptr;
   p.sw = scales ? scales->sw : nullptr;
-  p.counters = split > 1 ? static_cast<uint32_t*>(h->ws) : nullptr;
-  p.ws = split > 1 ? reinterpret_cast<float*>(static_cast<char*>(h->ws) + counters_bytes(h->ws_cap_tiles))
-                   : nullptr;
+  p.ws = split > 1 ? ws : nullptr;
+  p.counters = split > 1 ? counters : nullptr;
   p.status = h->d_status;
   p.M = int32_t(M);
   p.N = int32_t(h->N);
   p.K = int32_t(h->K);
-  p.m_tiles = int32_t(m_tiles);
+  p.m_tiles = int32_t(sh.m_tiles);
   p.n_tiles = int32_t(h->n_tiles);
   p.splits = split;
   p.kblocks = h->kblocks;
+  p.a_box_rows = int32_t(a_box_rows);
+  // L2 prefetch of W is off unless the handle asks for it: measured on GB300 it delayed the
+  // first loads more than it hid latency.
+  p.prefetch_kb = h->prefetch_kb > 0 ? h->prefetch_kb : 0;
   p.timeout_ns = h->timeout_ns;
   p.test_flags = test_flags;
 
-  const int64_t units = tiles * split;
-  const int grid = int(std::min<int64_t>(units, h->max_ctas));
+  const int64_t units = sh.tiles * split;
+  const int groups = int(std::min<int64_t>(units, h->max_groups));
   void* args[3] = {&tmap_x, &h->tmap_w, &p};
-  cudaError_t e = cudaLaunchKernel(h->kern.fn, dim3(grid), dim3(h->kern.threads), args,
-                                   size_t(h->kern.smem), st);
-  if (e != cudaSuccess) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(unsigned(groups * h->kern.ctas));
+  cfg.blockDim = dim3(unsigned(h->kern.threads));
+  cfg.dynamicSmemBytes = size_t(h->kern.smem);
+  cfg.stream = st;
+  // Programmatic dependent launch: the kernel's set-up may overlap the previous kernel's tail;
+  // it waits (griddepcontrol.wait) for that kernel to complete before touching global memory.
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (h->kern.ctas > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = unsigned(h->kern.ctas);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  if (cudaLaunchKernelExC(&cfg, h->kern.fn, args) != cudaSuccess) {
     cudaGetLastError();
     return BI_GEMM_ERR_CUDA;
   }
   return BI_GEMM_OK;
+}
+
+// Launch one run with the handle's workspace; `split_override` > 0 replaces the handle's split
+// count (control build only).
+int launch(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_gemm_scales* scales,
+           void* y, cudaStream_t st, int split_override, uint32_t test_flags) {
+  const int split = split_override > 0 ? split_override : h->split;
+  const Shape sh = shape_of(h, M);
+  int rc = ensure_workspace(h, sh.subtiles, split, st);
+  if (rc != BI_GEMM_OK) return rc;
+  uint32_t* counters = split > 1 ? static_cast<uint32_t*>(h->ws) : nullptr;
+  float* ws = split > 1 ? reinterpret_cast<float*>(static_cast<char*>(h->ws) + counters_bytes(h->ws_cap_tiles))
+                        : nullptr;
+  return launch_core(h, x, M, W, scales, y, st, split, ws, counters, test_flags);
 }
 
 int validate_run(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_gemm_scales* scales,
@@ -284,11 +347,10 @@ BI_GEMM_API int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtyp
   *out = nullptr;
   int rc = check_shape(K, N, dtype, scale_layout);
   if (rc != BI_GEMM_OK) return rc;
-  const int bn = block_n_for(N, dtype);
   const int bk = dtype == BI_MXFP8E4M3_OUT_BF16 ? 128 : 64;
   const int64_t kblocks = (K + bk - 1) / bk;
-  const int64_t n_tiles = (N + bn - 1) / bn;
-  if (opt && (opt->split_k < 0 || opt->split_k > kblocks || opt->max_ctas < 0))
+  if (opt && (opt->split_k < 0 || opt->split_k > kblocks || opt->max_ctas < 0 ||
+              opt->prefetch_kb < -1 || opt->prefetch_kb > 1024))
     return BI_GEMM_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -305,6 +367,8 @@ BI_GEMM_API int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtyp
   }
   if (major != 10 || minor != 3) return BI_GEMM_ERR_UNSUPPORTED;
   if (!encode_fn()) return BI_GEMM_ERR_CUDA;
+  const int bn = block_n_for(N, dtype, sms);
+  const int64_t n_tiles = (N + bn - 1) / bn;
 
   bi_gemm* h = new (std::nothrow) bi_gemm();
   if (!h) return BI_GEMM_ERR_OOM;
@@ -314,12 +378,14 @@ BI_GEMM_API int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtyp
   h->scale_layout = scale_layout;
   h->device = dev;
   h->num_sms = sms;
-  h->max_ctas = (opt && opt->max_ctas > 0) ? std::min(opt->max_ctas, sms) : sms;
   h->kern = select_kernel(dtype, bn);
+  h->max_ctas = (opt && opt->max_ctas > 0) ? std::min(opt->max_ctas, sms) : sms;
+  h->max_ctas = std::max(h->max_ctas, h->kern.ctas);
   h->kblocks = int(kblocks);
   h->n_tiles = int(n_tiles);
   h->split = (opt && opt->split_k > 0) ? opt->split_k : auto_split(n_tiles, kblocks, sms);
   h->timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+  h->prefetch_kb = (opt && opt->prefetch_kb != 0) ? std::max(0, opt->prefetch_kb) : -1;
   if (cudaFuncSetAttribute(h->kern.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->kern.smem) !=
           cudaSuccess ||
       cudaMalloc(&h->d_status, sizeof(uint32_t)) != cudaSuccess ||
@@ -328,6 +394,30 @@ BI_GEMM_API int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtyp
     if (h->d_status) cudaFree(h->d_status);
     delete h;
     return BI_GEMM_ERR_CUDA;
+  }
+  h->max_groups = h->max_ctas / h->kern.ctas;
+  if (h->kern.ctas > 1) {
+    // pairs that can be resident at once (one pair per two SMs unless the GPCs say otherwise)
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(unsigned(sms));
+    cfg.blockDim = dim3(unsigned(h->kern.threads));
+    cfg.dynamicSmemBytes = size_t(h->kern.smem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(h->kern.ctas);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, h->kern.fn, &cfg) != cudaSuccess || clusters < 1) {
+      cudaGetLastError();
+      cudaFree(h->d_status);
+      delete h;
+      return BI_GEMM_ERR_UNSUPPORTED;
+    }
+    h->max_groups = std::max(1, std::min(h->max_groups, clusters));
   }
   *out = h;
   return BI_GEMM_OK;
@@ -378,10 +468,10 @@ BI_GEMM_API int bi_gemm_destroy(bi_gemm_t h) {
 
 BI_GEMM_API int bi_gemm_get_config(bi_gemm_t h, bi_gemm_config* c) {
   if (!h || !c) return BI_GEMM_ERR_INVALID_ARG;
-  c->block_m = kBM;
+  c->block_m = kBM * h->kern.ctas;
   c->block_n = h->kern.bn;
   c->block_k = h->kern.bk;
-  c->mma_m = kBM;
+  c->mma_m = kBM * h->kern.ctas;
   c->mma_n = h->kern.bn;
   c->mma_k = h->kern.mma_k;
   c->stages = h->kern.stages;
@@ -391,6 +481,8 @@ BI_GEMM_API int bi_gemm_get_config(bi_gemm_t h, bi_gemm_config* c) {
   c->threads = h->kern.threads;
   c->smem_bytes = h->kern.smem;
   c->tmem_cols = h->kern.tmem_cols;
+  c->ctas_per_tile = h->kern.ctas;
+  c->max_groups = h->max_groups;
   return BI_GEMM_OK;
 }
 
@@ -400,7 +492,7 @@ BI_GEMM_API int bi_gemm_workspace_size(bi_gemm_t h, int64_t M, uint64_t* bytes) 
     *bytes = 0;
     return BI_GEMM_OK;
   }
-  const int64_t tiles = ((M + kBM - 1) / kBM) * h->n_tiles;
+  const int64_t tiles = shape_of(h, M).subtiles;
   *bytes = counters_bytes(tiles) + size_t(tiles) * h->split * kBM * h->kern.bn * sizeof(float);
   return BI_GEMM_OK;
 }
@@ -477,63 +569,25 @@ BI_GEMM_API int bi_gemm_run_noalloc(bi_gemm_t h, const void* x, int64_t M, const
   }
   if (dev != h->device) return BI_GEMM_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool fp8 = h->dtype == BI_MXFP8E4M3_OUT_BF16;
   const int split = h->split;
-  const int64_t m_tiles = (M + kBM - 1) / kBM;
-  const int64_t tiles = m_tiles * h->n_tiles;
-  if (tiles * split >= (int64_t(1) << 31)) return BI_GEMM_ERR_UNSUPPORTED;
+  const Shape sh = shape_of(h, M);
   char* scratch = nullptr;
   if (split > 1) {
-    const size_t part = size_t(tiles) * split * kBM * h->kern.bn * sizeof(float);
-    if (size_t(tiles) * sizeof(uint32_t) > kNoAllocCounterBytes ||
+    const size_t part = size_t(sh.subtiles) * split * kBM * h->kern.bn * sizeof(float);
+    if (size_t(sh.subtiles) * sizeof(uint32_t) > kNoAllocCounterBytes ||
         part > kNoAllocScratchBytes - kNoAllocCounterBytes)
       return BI_GEMM_ERR_SCRATCH_LIMIT;
     rc = noalloc_scratch_address(dev, &scratch);
     if (rc != BI_GEMM_OK) return rc;
-  }
-
-  CUtensorMap tmap_x;
-  if (!encode_2d(&tmap_x, x, fp8, uint64_t(M), uint64_t(h->K), kBM, 128 / (fp8 ? 1 : 2)))
-    return BI_GEMM_ERR_CUDA;
-  if (h->w_cached != W) {
-    if (!encode_2d(&h->tmap_w, W, fp8, uint64_t(h->K), uint64_t(h->N), h->kern.bk,
-                   128 / (fp8 ? 1 : 2))) {
-      h->w_cached = nullptr;
+    // The previous call's counters are normally back at zero, but an aborted run can leave
+    // them set: clear the ones this call uses.  Partials need no clearing (written before read).
+    if (cudaMemsetAsync(scratch, 0, size_t(sh.subtiles) * sizeof(uint32_t), st) != cudaSuccess) {
+      cudaGetLastError();
       return BI_GEMM_ERR_CUDA;
     }
-    h->w_cached = W;
   }
-  // The previous call's counters are normally back at zero, but an aborted run can leave them
-  // set: clear the ones this call uses.  Partials need no clearing (written before read).
-  if (split > 1 && cudaMemsetAsync(scratch, 0, size_t(tiles) * sizeof(uint32_t), st) != cudaSuccess) {
-    cudaGetLastError();
-    return BI_GEMM_ERR_CUDA;
-  }
-
-  KParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.y = y;
-  p.sx = scales ? scales->sx : nullptr;
-  p.sw = scales ? scales->sw : nullptr;
-  p.counters = split > 1 ? reinterpret_cast<uint32_t*>(scratch) : nullptr;
-  p.ws = split > 1 ? reinterpret_cast<float*>(scratch + kNoAllocCounterBytes) : nullptr;
-  p.status = h->d_status;
-  p.M = int32_t(M);
-  p.N = int32_t(h->N);
-  p.K = int32_t(h->K);
-  p.m_tiles = int32_t(m_tiles);
-  p.n_tiles = int32_t(h->n_tiles);
-  p.splits = split;
-  p.kblocks = h->kblocks;
-  p.timeout_ns = h->timeout_ns;
-  p.test_flags = 0u;
-  const int grid = int(std::min<int64_t>(tiles * split, h->max_ctas));
-  void* args[3] = {&tmap_x, &h->tmap_w, &p};
-  if (cudaLaunchKernel(h->kern.fn, dim3(grid), dim3(h->kern.threads), args, size_t(h->kern.smem), st) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    return BI_GEMM_ERR_CUDA;
-  }
-  return BI_GEMM_OK;
+  return launch_core(h, x, M, W, scales, y, st, split,
+                     split > 1 ? reinterpret_cast<float*>(scratch + kNoAllocCounterBytes) : nullptr,
+                     split > 1 ? reinterpret_cast<uint32_t*>(scratch) : nullptr, 0u);
 }
 #endif

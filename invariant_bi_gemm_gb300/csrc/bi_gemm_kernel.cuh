@@ -18,6 +18,11 @@
 // The persistent tile order (which SM computes which tile, and when) does change with M,
 // but it decides no arithmetic: a tile's value is the same wherever it runs.
 //
+// Tile = 128 x BN per CTA, or 256 x BN per CTA pair (CTAS = 2, BN = 256): the pair issues one
+// tcgen05.mma.cta_group::2 of M=256, each CTA staging its own 128 rows of x and its own BN/2
+// columns of W and receiving its 128 rows of the accumulator in its own TMEM.  The pair is one
+// fixed configuration chosen from N, like everything else.
+//
 // Warp roles (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer: x tile [128 x BK] (K-major, 128-byte swizzle) and W tile
 //               [BK x BN] (N-major, 128-byte swizzle) per pipeline stage;
@@ -57,6 +62,8 @@ struct KParams {
   int32_t m_tiles, n_tiles;
   int32_t splits;           // S
   int32_t kblocks;          // KB = ceil(K / BK)
+  int32_t a_box_rows;       // rows per x TMA box: 128, or round_up(M, 8) when M < 128
+  int32_t prefetch_kb;      // W k-blocks requested into L2 ahead of the ring (0 = none)
   uint64_t timeout_ns;
   uint32_t test_flags;      // only read by the control build
 };
@@ -67,22 +74,31 @@ constexpr __host__ __device__ int pow2_ceil(int v) {
   return p;
 }
 
-template <bool kFp8_, bool kOutF32_, int kBN_, int kStages_, int kAccBufs_>
+template <bool kFp8_, bool kOutF32_, int kBN_, int kStages_, int kAccBufs_, int kCtas_ = 1>
 struct KCfg {
   static constexpr bool kFp8 = kFp8_;
   static constexpr bool kOutF32 = kOutF32_;
   static constexpr int BN = kBN_;
   static constexpr int STAGES = kStages_;
   static constexpr int ACC_BUFS = kAccBufs_;
+  static constexpr int CTAS = kCtas_;                   // CTAs per output tile (1 or 2)
+  static_assert(CTAS == 1 || (CTAS == 2 && !kFp8_ && (kBN_ == 256 || kBN_ == 192)),
+                "CTA pairs: bf16, BN = 256 or 192");
+  static constexpr int TILE_M = kBM * CTAS;
+  static constexpr int BN_CTA = BN / CTAS;              // W columns staged by each CTA
   static constexpr int ELEM = kFp8 ? 1 : 2;
   static constexpr int BK = 128 / ELEM;                 // one 128-byte swizzle row of K
   static constexpr int MMA_K = kFp8 ? 32 : 16;          // K per tcgen05.mma
   static constexpr int K_STEPS = BK / MMA_K;            // 4
-  static constexpr int ATOM_N = 128 / ELEM;             // N per 128-byte swizzle row of W
-  static constexpr int N_ATOMS = BN / ATOM_N;
-  static_assert(BN % ATOM_N == 0 && BN >= 16 && BN <= 256, "BN");
+  // W is staged N-major in 128-byte swizzle atoms (64 bf16 / 128 E4M3 columns), or 64-byte
+  // atoms (32 bf16 columns) when a CTA's share of the tile is not a multiple of 64 columns.
+  static constexpr int B_SW = (BN_CTA * ELEM) % 128 == 0 ? 128 : 64;   // swizzle span in bytes
+  static constexpr int ATOM_N = B_SW / ELEM;             // N per swizzle row of W
+  static constexpr int N_ATOMS = BN_CTA / ATOM_N;        // swizzle atoms of W per CTA
+  static_assert(BN_CTA % ATOM_N == 0 && BN >= 16 && BN <= 256, "BN");
+  static constexpr uint32_t B_LAYOUT = B_SW == 128 ? 2u : 4u;   // descriptor layout code
   static constexpr int A_BYTES = kBM * 128;             // 16 KB
-  static constexpr int B_ATOM_BYTES = BK * 128;
+  static constexpr int B_ATOM_BYTES = BK * B_SW;
   static constexpr int B_BYTES = N_ATOMS * B_ATOM_BYTES;
   static constexpr int SFA_BYTES = kFp8 ? 512 : 0;      // 128 rows x 4 k-blocks
   static constexpr int SFB_BYTES = kFp8 ? (BN / 128) * 512 : 0;
@@ -90,7 +106,6 @@ struct KCfg {
   static constexpr int NUM_WARPS = kFp8 ? 7 : 6;
   static constexpr int EPI_WARP0 = NUM_WARPS - 4;
   static constexpr int THREADS = NUM_WARPS * 32;
-  static constexpr int TX_BYTES = A_BYTES + B_BYTES;
   // TMEM columns: accumulators first, then 16 columns of scale factors per stage.
   static constexpr int SF_TMEM_COL0 = ACC_BUFS * BN;
   static constexpr int TMEM_USED = SF_TMEM_COL0 + (kFp8 ? 16 * STAGES : 0);
@@ -109,7 +124,7 @@ struct KCfg {
   // tcgen05 instruction descriptor (kind::f16): D=f32, A=B=bf16, A K-major, B N-major.
   static constexpr uint32_t IDESC_BF16 =
       (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
-      (uint32_t(BN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+      (uint32_t(BN >> 3) << 17) | (uint32_t(TILE_M >> 4) << 24);
   // tcgen05 instruction descriptor (kind::mxf8f6f4 block-scaled): A=B=E4M3, A K-major,
   // B N-major, E8M0 scales; the scale-factor byte selectors are OR-ed in per K step.
   static constexpr uint32_t IDESC_MXF8 =
@@ -185,6 +200,7 @@ template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     bi_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w, const KParams p) {
+  constexpr bool kPair = C::CTAS == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -203,6 +219,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;   // 0 = leader (issues the MMAs)
+  const int group = blockIdx.x / C::CTAS;                        // this CTA's tile group
+  const int ngroups = gridDim.x / C::CTAS;
   const int units = p.m_tiles * p.n_tiles * p.splits;
 
   if (threadIdx.x == 0) {
@@ -212,7 +231,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     for (int b = 0; b < C::ACC_BUFS; ++b) {
       ptx::mbar_init(tfull_bar(b), 1u);
-      ptx::mbar_init(tempty_bar(b), 4u);
+      ptx::mbar_init(tempty_bar(b), 4u * C::CTAS);
     }
     ptx::mbar_init(drain_bar, 1u);
     ptx::mbar_init(epi_bar, 4u);
@@ -224,25 +243,50 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     ptx::prefetch_tensormap(&tmap_w);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (kPair) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
+  // Pairs: announce "barriers initialised, TMEM allocated" to the peer now, and wait for the
+  // peer's announcement only where it matters (before touching the peer's barriers or TMEM).
+  if constexpr (kPair) ptx::cluster_arrive();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const SyncCtx sc{abort_flag, p.status, p.timeout_ns};
+  // Everything above touched only this CTA's shared memory and TMEM, so it may overlap the
+  // tail of the previous kernel in the stream; global memory is read or written only after
+  // that kernel has completed.
+  ptx::grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    if constexpr (kPair) {
+      if (lane != 0 || rank != 0) ptx::cluster_wait();   // the peer signals the leader's barriers
+    }
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_par = 0;   // per stage: an issue is outstanding / its parity
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int u = group; u < units && ok; u += ngroups) {
         const UnitCoord uc = unit_coord(u, p);
+        const int wcol0 = uc.n_tile * C::BN + int(rank) * C::BN_CTA;
+        auto prefetch_w = [&](int kb) {
+#pragma unroll
+          for (int a = 0; a < C::N_ATOMS; ++a) ptx::tma_prefetch_2d(&tmap_w, wcol0 + a * C::ATOM_N, kb * C::BK);
+        };
+        // W k-blocks are requested into L2 ahead of the ring so that HBM stays busy when only a
+        // few CTAs stream W (small M); the hint changes no data and no arithmetic.
+        const int pf = p.prefetch_kb;
+        for (int kb = uc.kb_begin; kb < min(uc.kb_end, uc.kb_begin + pf); ++kb) prefetch_w(kb);
         for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
+          if (pf > 0 && kb + pf < uc.kb_end) prefetch_w(kb + pf);
           if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
             ok = false;
             break;
@@ -250,18 +294,38 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           bool skip = false;
 #ifdef BI_GEMM_CONTROLS
           // control build only: withhold one stage so that the consumer's bounded wait expires
-          skip = (p.test_flags & 1u) && u == (int)blockIdx.x && kb == uc.kb_begin;
+          skip = (p.test_flags & 1u) && u == group && kb == uc.kb_begin;
 #endif
           if (!skip) {
             const uint32_t fb = full_bar(stage);
-            ptx::mbar_arrive_expect_tx(fb, C::TX_BYTES);
-            ptx::tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmap_x, fb, kb * C::BK,
-                             uc.m_tile * kBM);
+            const uint32_t adst = sbase + C::OFF_A + stage * C::A_BYTES;
             const uint32_t bdst = sbase + C::OFF_B + stage * C::B_BYTES;
+            const int row0 = uc.m_tile * C::TILE_M + int(rank) * kBM;
+            const int col0 = uc.n_tile * C::BN + int(rank) * C::BN_CTA;
+            // x rows at or past M are never stored, so they need not be loaded: a CTA whose 128
+            // rows all lie past M skips its x tile, and the x box is only as tall as M needs.
+            // The shared-memory rows left unwritten feed only those discarded output rows.
+            const uint32_t a_bytes = uint32_t(p.a_box_rows) * 128u;
+            const bool load_a = row0 < p.M;
+            if constexpr (kPair) {
+              const uint32_t lfb = ptx::mapa_shared(fb, 0);   // the leader's full barrier
+              if (rank == 0) {
+                const bool peer_a = row0 + kBM < p.M;
+                ptx::mbar_arrive_expect_tx(fb, (load_a ? a_bytes : 0u) + (peer_a ? a_bytes : 0u) +
+                                                   uint32_t(C::CTAS * C::B_BYTES));
+              }
+              if (load_a) ptx::tma_load_2d_pair(adst, &tmap_x, lfb, kb * C::BK, row0);
 #pragma unroll
-            for (int a = 0; a < C::N_ATOMS; ++a)
-              ptx::tma_load_2d(bdst + a * C::B_ATOM_BYTES, &tmap_w, fb,
-                               uc.n_tile * C::BN + a * C::ATOM_N, kb * C::BK);
+              for (int a = 0; a < C::N_ATOMS; ++a)
+                ptx::tma_load_2d_pair(bdst + a * C::B_ATOM_BYTES, &tmap_w, lfb, col0 + a * C::ATOM_N,
+                                      kb * C::BK);
+            } else {
+              ptx::mbar_arrive_expect_tx(fb, a_bytes + uint32_t(C::B_BYTES));
+              ptx::tma_load_2d(adst, &tmap_x, fb, kb * C::BK, row0);
+#pragma unroll
+              for (int a = 0; a < C::N_ATOMS; ++a)
+                ptx::tma_load_2d(bdst + a * C::B_ATOM_BYTES, &tmap_w, fb, col0 + a * C::ATOM_N, kb * C::BK);
+            }
             issued_mask |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           }
@@ -271,26 +335,38 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
         }
       }
+      ptx::launch_dependents();   // this CTA has issued all its loads
+      if constexpr (kPair) {
+        if (rank == 0) ptx::cluster_wait();
+      }
       if (!ok) {
         // let every copy already in flight land before the CTA can exit
-        SyncCtx drain{abort_flag, p.status, p.timeout_ns};
-        volatile uint32_t no_abort = 0;
-        drain.abort = &no_abort;
-        for (int s = 0; s < C::STAGES; ++s)
-          if (issued_mask & (1u << s))
-            wait_phase(full_bar(s), (issued_par >> s) & 1u, drain, kErrTimeoutProducer);
+        if (rank == 0) {
+          SyncCtx drain{abort_flag, p.status, p.timeout_ns};
+          volatile uint32_t no_abort = 0;
+          drain.abort = &no_abort;
+          for (int s = 0; s < C::STAGES; ++s)
+            if (issued_mask & (1u << s))
+              wait_phase(full_bar(s), (issued_par >> s) & 1u, drain, kErrTimeoutProducer);
+        } else if (issued_mask) {
+          // the peer's copies are counted on the leader's barriers: give them time to land
+          const uint64_t t0 = ptx::globaltimer();
+          while (ptx::globaltimer() - t0 < 2000000ull) {
+          }
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (leader CTA)
+    if constexpr (kPair) ptx::cluster_wait();            // the peer's TMEM is allocated
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
       uint32_t bphase = 0;
       bool ok = true, issued_any = false;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int u = group; u < units && ok; u += ngroups) {
         const UnitCoord uc = unit_coord(u, p);
         if (!wait_phase(tempty_bar(buf), bphase ^ 1u, sc, kErrTimeoutMma)) {
           ok = false;
@@ -318,8 +394,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < C::K_STEPS; ++kk) {
               const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
-              const uint64_t bd =
-                  make_sdesc(b_addr + kk * C::MMA_K * 128, C::B_ATOM_BYTES, 1024, kLayoutSW128);
+              const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
+                                             8 * C::B_SW, C::B_LAYOUT);
               const uint32_t idesc = C::IDESC_MXF8 | (uint32_t(kk) << 4) | (uint32_t(kk) << 29);
               ptx::mma_mxf8(d_tmem, ad, bd, idesc, sfa_t, sfb_t,
                             (kb != uc.kb_begin || kk != 0) ? 1u : 0u);
@@ -328,20 +404,30 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < C::K_STEPS; ++kk) {
               const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
-              const uint64_t bd =
-                  make_sdesc(b_addr + kk * C::MMA_K * 128, C::B_ATOM_BYTES, 1024, kLayoutSW128);
-              ptx::mma_bf16(d_tmem, ad, bd, C::IDESC_BF16, (kb != uc.kb_begin || kk != 0) ? 1u : 0u);
+              const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
+                                             8 * C::B_SW, C::B_LAYOUT);
+              const uint32_t acc = (kb != uc.kb_begin || kk != 0) ? 1u : 0u;
+              if constexpr (kPair)
+                ptx::mma_bf16_pair(d_tmem, ad, bd, C::IDESC_BF16, acc);
+              else
+                ptx::mma_bf16(d_tmem, ad, bd, C::IDESC_BF16, acc);
             }
           }
           issued_any = true;
-          ptx::tc_commit(empty_bar(stage));
+          if constexpr (kPair)
+            ptx::tc_commit_pair_mc(empty_bar(stage), 0x3);   // frees the stage in both CTAs
+          else
+            ptx::tc_commit(empty_bar(stage));
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::tc_commit(tfull_bar(buf));
+        if constexpr (kPair)
+          ptx::tc_commit_pair_mc(tfull_bar(buf), 0x3);       // both CTAs' epilogues
+        else
+          ptx::tc_commit(tfull_bar(buf));
         if (++buf == C::ACC_BUFS) {
           buf = 0;
           bphase ^= 1u;
@@ -349,7 +435,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       if (!ok && issued_any) {
         // wait for the MMAs already issued before TMEM is released
-        ptx::tc_commit(drain_bar);
+        if constexpr (kPair)
+          ptx::tc_commit_pair_mc(drain_bar, 0x1);
+        else
+          ptx::tc_commit(drain_bar);
         SyncCtx drain{abort_flag, p.status, p.timeout_ns};
         volatile uint32_t no_abort = 0;
         drain.abort = &no_abort;
@@ -359,6 +448,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncwarp();
   } else if (C::kFp8 && warp == 2) {
     // ------------------------------------------------------------ scale producer (MXFP8)
+    if constexpr (kPair) ptx::cluster_wait();
     // Layout expected by tcgen05.cp 32x128b.warpx4 for 128 rows x 4 k-blocks (512 bytes):
     // byte (r % 32) * 16 + (r / 32) * 4 + kblk.  One 512-byte block for x's rows, one per
     // 128 columns of W.
@@ -366,7 +456,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t phase = 0;
     const int KB32 = p.K / 32;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    for (int u = group; u < units && ok; u += ngroups) {
       const UnitCoord uc = unit_coord(u, p);
       for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
         if (!warp_wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutScales)) {
@@ -411,58 +501,74 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncwarp();
   } else if (warp >= C::EPI_WARP0) {
     // ------------------------------------------------------------ epilogue
+    if constexpr (kPair) ptx::cluster_wait();
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int epi_tid = (warp - C::EPI_WARP0) * 32 + lane;
     int buf = 0;
     uint32_t bphase = 0, ephase = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    for (int u = group; u < units; u += ngroups) {
       const UnitCoord uc = unit_coord(u, p);
       if (!warp_wait_phase(tfull_bar(buf), bphase, sc, kErrTimeoutEpilogue)) break;
       ptx::tc_fence_after();
-      const int row_in_tile = q * 32 + lane;
-      const int row = uc.m_tile * kBM + row_in_tile;
+      const int row_in_tile = q * 32 + lane;                       // row within this CTA's 128
+      const int row = uc.m_tile * C::TILE_M + int(rank) * kBM + row_in_tile;
       const int col_tile0 = uc.n_tile * C::BN;
-#pragma unroll 1
-      for (int c = 0; c < C::BN / 32; ++c) {
+      const int sub = uc.tile * C::CTAS + int(rank);               // split-K sub-tile index
+      const bool warp_has_rows = row - lane < p.M;                 // warp-uniform
+      // Convert and store 32 accumulator columns of this thread's row.
+      auto store_chunk = [&](int c, const uint32_t (&r)[32]) {
         const int col0 = col_tile0 + c * 32;
-        if (col0 >= p.N) break;             // uniform across the warp
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(tmem_base + uint32_t(buf * C::BN + c * 32) + (uint32_t(q * 32) << 16), r);
-        ptx::tmem_wait_ld();
         const int nvalid = min(32, p.N - col0);
-        if (row < p.M) {
-          if (p.splits > 1) {
-            float* dst = p.ws + ((((size_t)uc.tile * p.splits + uc.s) * kBM + row_in_tile) * C::BN + c * 32);
+        if (row >= p.M) return;
+        if (p.splits > 1) {
+          float* dst = p.ws + ((((size_t)sub * p.splits + uc.s) * kBM + row_in_tile) * C::BN + c * 32);
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              if (v * 4 < nvalid) ptx::st_global_v4(dst + v * 4, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-          } else if constexpr (C::kOutF32) {
-            float* dst = reinterpret_cast<float*>(p.y) + (size_t)row * p.N + col0;
+          for (int v = 0; v < 8; ++v)
+            if (v * 4 < nvalid) ptx::st_global_v4(dst + v * 4, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        } else if constexpr (C::kOutF32) {
+          float* dst = reinterpret_cast<float*>(p.y) + (size_t)row * p.N + col0;
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              if (v * 4 < nvalid) ptx::st_global_v4(dst + v * 4, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-          } else {
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)row * p.N + col0;
+          for (int v = 0; v < 8; ++v)
+            if (v * 4 < nvalid) ptx::st_global_v4(dst + v * 4, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        } else {
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)row * p.N + col0;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              if (v * 8 < nvalid) {
-                const float* f = reinterpret_cast<const float*>(r + 8 * v);
-                ptx::st_global_v4(dst + v * 8, ptx::pack_bf16x2(f[0], f[1]), ptx::pack_bf16x2(f[2], f[3]),
-                                  ptx::pack_bf16x2(f[4], f[5]), ptx::pack_bf16x2(f[6], f[7]));
-              }
+          for (int v = 0; v < 4; ++v) {
+            if (v * 8 < nvalid) {
+              const float* f = reinterpret_cast<const float*>(r + 8 * v);
+              ptx::st_global_v4(dst + v * 8, ptx::pack_bf16x2(f[0], f[1]), ptx::pack_bf16x2(f[2], f[3]),
+                                ptx::pack_bf16x2(f[4], f[5]), ptx::pack_bf16x2(f[6], f[7]));
             }
           }
         }
+      };
+      const uint32_t trow = tmem_base + uint32_t(buf * C::BN) + (uint32_t(q * 32) << 16);
+      // Two 32-column TMEM loads per wait; a warp whose 32 rows all lie past M reads nothing.
+#pragma unroll 1
+      for (int c = 0; c < C::BN / 32; c += 2) {
+        if (col_tile0 + c * 32 >= p.N || !warp_has_rows) break;   // uniform across the warp
+        uint32_t r0[32], r1[32];
+        const bool two = c + 1 < C::BN / 32 && col_tile0 + (c + 1) * 32 < p.N;
+        ptx::tmem_ld_32x32b_x32(trow + uint32_t(c * 32), r0);
+        if (two) ptx::tmem_ld_32x32b_x32(trow + uint32_t((c + 1) * 32), r1);
+        ptx::tmem_wait_ld();
+        store_chunk(c, r0);
+        if (two) store_chunk(c + 1, r1);
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
+      if (lane == 0) {
+        if constexpr (kPair)
+          ptx::mbar_arrive_remote(ptx::mapa_shared(tempty_bar(buf), 0));   // the leader's barrier
+        else
+          ptx::mbar_arrive(tempty_bar(buf));
+      }
       if (++buf == C::ACC_BUFS) {
         buf = 0;
         bphase ^= 1u;
       }
       if (p.splits > 1) {
-        // Fixed-order merge of the S partials by the last CTA to arrive at this tile.
+        // Fixed-order merge of the S partials by the last CTA to arrive at this sub-tile.
         // Hand-off 1: every partial of this CTA is stored and fenced before the count.
         __threadfence();
         __syncwarp();
@@ -470,7 +576,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!warp_wait_phase(epi_bar, ephase, sc, kErrTimeoutEpilogue)) break;
         ephase ^= 1u;
         if (epi_tid == 0) {
-          const uint32_t old = atomicAdd(p.counters + uc.tile, 1u);
+          const uint32_t old = atomicAdd(p.counters + sub, 1u);
           *last_flag = (old == uint32_t(p.splits - 1)) ? 1u : 0u;
         }
         // Hand-off 2: the verdict is visible to all four warps.
@@ -482,7 +588,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (last) {
           __threadfence();
           if (row < p.M) {
-            const float* src0 = p.ws + (((size_t)uc.tile * p.splits) * kBM + row_in_tile) * C::BN;
+            const float* src0 = p.ws + (((size_t)sub * p.splits) * kBM + row_in_tile) * C::BN;
             const size_t sstride = (size_t)kBM * C::BN;
 #pragma unroll 1
             for (int c = 0; c < C::BN / 32; ++c) {
@@ -515,7 +621,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               }
             }
           }
-          if (epi_tid == 0) p.counters[uc.tile] = 0u;   // ready for the next launch
+          if (epi_tid == 0) p.counters[sub] = 0u;   // ready for the next launch
         }
         // Hand-off 3: last_flag may be rewritten only after every warp has read it.
         __syncwarp();
@@ -528,9 +634,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) ptx::cluster_sync();   // neither CTA leaves while the pair still works
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (kPair)
+      ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 

@@ -39,7 +39,8 @@ def setup():
 
 def test_config(setup):
     c = setup[0].config
-    assert (c["block_m"], c["block_n"], c["mma_n"], c["split_k"]) == (128, 256, 256, 1)
+    assert (c["block_m"], c["block_n"], c["mma_m"], c["mma_n"], c["split_k"], c["ctas_per_tile"]) == \
+        (256, 256, 256, 256, 1, 2)
 
 
 def test_rows_bitwise_identical_across_m(setup):

@@ -28,6 +28,8 @@ def test_empty_batch_is_noop():
     (1032, 264, "bf16", 257),      # N just above one 256 tile
     (4096, 520, "bf16_f32", 300),
     (8, 64, "bf16", 1),            # K = 8: one partial k-block
+    (1024, 4000, "bf16", 300),     # N ends inside the second (peer) half of the last pair tile
+    (1024, 4000, "bf16_f32", 77),
 ])
 def test_ragged_shapes(K, N, kind, M):
     x = ig.normal_bf16(21, M, K)
@@ -125,4 +127,23 @@ def test_workspace_size_reported():
     assert g.workspace_size(0) == 0
     assert g.workspace_size(256) >= 2 * 32 * 128 * 64 * 4
     assert BiGemm(4096, 14336, "bf16").workspace_size(8192) == 0
+    g.close()
+
+
+@pytest.mark.parametrize("kind,out", [("bf16", "bf16"), ("bf16_f32", "f32")])
+def test_forced_split_on_pair_tile(kind, out):
+    """A fixed split count on the 256 x 256 CTA-pair tile: each CTA merges its own 128 rows."""
+    K, N, M = 4096, 512, 300
+    x = ig.normal_bf16(81, M, K)
+    w = ig.normal_bf16(82, K, N, std=0.02)
+    y_ref, _, sabs = oracle.gemm_bf16(x, w, out)
+    g = BiGemm(K, N, kind, split_k=4)
+    assert g.config["ctas_per_tile"] == 2 and g.config["split_k"] == 4
+    xd, wd = dev_bf16(x), dev_bf16(w)
+    y = host_bits(g(xd, wd))
+    check_tolerance(y, y_ref, sabs, oracle.TOL_F32 if out == "f32" else oracle.TOL_BF16, "pair split")
+    for M2 in (1, 129, 257):
+        y2 = host_bits(g(xd[:M2].contiguous(), wd))
+        assert np.array_equal(y2.view(np.uint8), y[:M2].view(np.uint8)), M2
+    assert g.device_error() == 0
     g.close()
