@@ -92,10 +92,6 @@ typedef struct {
                              count (1 <= split_k <= ceil(K / BK)); still never M-dependent */
   int32_t max_ctas;       /* 0 = one CTA per SM; otherwise an upper bound on the grid     */
   uint64_t timeout_ns;    /* 0 = default (5 s); limit of every in-kernel wait             */
-  int32_t prefetch_kb;    /* L2 prefetch distance of W in K stages: 0 or -1 = none (the
-                             default), 1..1024 = request W this many stages ahead of the
-                             shared-memory ring.  A memory hint only: results are bitwise
-                             the same for every setting.                                  */
 } bi_gemm_options;
 
 /* bi_gemm_create with explicit options (NULL = defaults, same as bi_gemm_create). */

@@ -50,8 +50,7 @@ class bi_gemm_scales(ctypes.Structure):
 
 
 class bi_gemm_options(ctypes.Structure):
-    _fields_ = [("split_k", ctypes.c_int32), ("max_ctas", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
-                ("prefetch_kb", ctypes.c_int32)]
+    _fields_ = [("split_k", ctypes.c_int32), ("max_ctas", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64)]
 
 
 class bi_gemm_config(ctypes.Structure):
@@ -177,13 +176,13 @@ class BiGemm:
     """
 
     def __init__(self, K: int, N: int, kind: str = "bf16", split_k: int = 0, max_ctas: int = 0,
-                 timeout_ns: int = 0, prefetch_kb: int = 0):
+                 timeout_ns: int = 0):
         self.K, self.N, self.kind = int(K), int(N), kind
         self.dtype = _DTYPES[kind]
         layout = BI_SCALES_E8M0_K32 if kind == "mxfp8" else BI_SCALES_NONE
         opts = None
-        if split_k or max_ctas or timeout_ns or prefetch_kb:
-            opts = bi_gemm_options(int(split_k), int(max_ctas), int(timeout_ns), int(prefetch_kb))
+        if split_k or max_ctas or timeout_ns:
+            opts = bi_gemm_options(int(split_k), int(max_ctas), int(timeout_ns))
         self.handle = bi_gemm_create(self.K, self.N, self.dtype, layout, opts)
 
     @property

@@ -104,20 +104,25 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D row-major [rows, cols] tensor, box [box_rows, box_cols], 128- or 64-byte swizzle, zero fill.
-static bool encode_2d(CUtensorMap* m, const void* base, bool u8, uint64_t rows, uint64_t cols,
+// 2-D row-major [rows, cols] tensor of 1-, 2- or 4-byte elements (uint8 / bf16 / fp32), box
+// [box_rows, box_cols], 128- or 64-byte swizzle (0 = none), zero fill for loads.
+static bool encode_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t rows, uint64_t cols,
                       uint32_t box_rows, uint32_t box_cols, int swizzle = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const uint64_t elem = u8 ? 1 : 2;
+  const uint64_t elem = uint64_t(elem_bytes);
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * elem};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                  const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUtensorMapDataType dt = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapSwizzle sw = swizzle == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -132,7 +137,6 @@ struct bi_gemm {
   int device = 0, num_sms = 0, max_ctas = 0;
   int split = 1, kblocks = 0, n_tiles = 0;
   int max_groups = 0;      // CTA groups (single CTAs or pairs) resident at once
-  int prefetch_kb = -1;    // < 0: automatic
   uint64_t timeout_ns = kDefaultTimeoutNs;
   KernelInfo kern;
   uint32_t* d_status = nullptr;
@@ -245,11 +249,16 @@ int launch_core(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_ge
 
   // x box: 128 rows, or only round_up(M, 8) rows when M < 128 (rows past M are never stored)
   const uint32_t a_box_rows = M >= kBM ? uint32_t(kBM) : uint32_t((M + 7) / 8 * 8);
-  CUtensorMap tmap_x;
-  if (!encode_2d(&tmap_x, x, fp8, uint64_t(M), uint64_t(h->K), a_box_rows, 128 / (fp8 ? 1 : 2)))
+  CUtensorMap tmap_x, tmap_y;
+  if (!encode_2d(&tmap_x, x, fp8 ? 1 : 2, uint64_t(M), uint64_t(h->K), a_box_rows, 128 / (fp8 ? 1 : 2)))
+    return BI_GEMM_ERR_CUDA;
+  // y: 32 x 32 output blocks staged with the swizzle that matches their row length
+  // (bf16: 64-byte rows, 64-byte swizzle; fp32: 128-byte rows, 128-byte swizzle)
+  const bool f32 = h->dtype == BI_BF16_OUT_F32;
+  if (!encode_2d(&tmap_y, y, f32 ? 4 : 2, uint64_t(M), uint64_t(h->N), 32, 32, f32 ? 128 : 64))
     return BI_GEMM_ERR_CUDA;
   if (h->w_cached != W) {
-    if (!encode_2d(&h->tmap_w, W, fp8, uint64_t(h->K), uint64_t(h->N), h->kern.bk,
+    if (!encode_2d(&h->tmap_w, W, fp8 ? 1 : 2, uint64_t(h->K), uint64_t(h->N), h->kern.bk,
                    uint32_t(h->kern.w_box_cols), h->kern.w_swizzle)) {
       h->w_cached = nullptr;
       return BI_GEMM_ERR_CUDA;
@@ -273,15 +282,12 @@ int launch_core(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_ge
   p.splits = split;
   p.kblocks = h->kblocks;
   p.a_box_rows = int32_t(a_box_rows);
-  // L2 prefetch of W is off unless the handle asks for it: measured on GB300 it delayed the
-  // first loads more than it hid latency.
-  p.prefetch_kb = h->prefetch_kb > 0 ? h->prefetch_kb : 0;
   p.timeout_ns = h->timeout_ns;
   p.test_flags = test_flags;
 
   const int64_t units = sh.tiles * split;
   const int groups = int(std::min<int64_t>(units, h->max_groups));
-  void* args[3] = {&tmap_x, &h->tmap_w, &p};
+  void* args[4] = {&tmap_x, &h->tmap_w, &tmap_y, &p};
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(unsigned(groups * h->kern.ctas));
@@ -349,8 +355,7 @@ BI_GEMM_API int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtyp
   if (rc != BI_GEMM_OK) return rc;
   const int bk = dtype == BI_MXFP8E4M3_OUT_BF16 ? 128 : 64;
   const int64_t kblocks = (K + bk - 1) / bk;
-  if (opt && (opt->split_k < 0 || opt->split_k > kblocks || opt->max_ctas < 0 ||
-              opt->prefetch_kb < -1 || opt->prefetch_kb > 1024))
+  if (opt && (opt->split_k < 0 || opt->split_k > kblocks || opt->max_ctas < 0))
     return BI_GEMM_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -385,7 +390,6 @@ BI_GEMM_API int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtyp
   h->n_tiles = int(n_tiles);
   h->split = (opt && opt->split_k > 0) ? opt->split_k : auto_split(n_tiles, kblocks, sms);
   h->timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
-  h->prefetch_kb = (opt && opt->prefetch_kb != 0) ? std::max(0, opt->prefetch_kb) : -1;
   if (cudaFuncSetAttribute(h->kern.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->kern.smem) !=
           cudaSuccess ||
       cudaMalloc(&h->d_status, sizeof(uint32_t)) != cudaSuccess ||

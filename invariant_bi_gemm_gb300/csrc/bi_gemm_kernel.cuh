@@ -63,7 +63,6 @@ struct KParams {
   int32_t splits;           // S
   int32_t kblocks;          // KB = ceil(K / BK)
   int32_t a_box_rows;       // rows per x TMA box: 128, or round_up(M, 8) when M < 128
-  int32_t prefetch_kb;      // W k-blocks requested into L2 ahead of the ring (0 = none)
   uint64_t timeout_ns;
   uint32_t test_flags;      // only read by the control build
 };
@@ -103,8 +102,10 @@ struct KCfg {
   static constexpr int SFA_BYTES = kFp8 ? 512 : 0;      // 128 rows x 4 k-blocks
   static constexpr int SFB_BYTES = kFp8 ? (BN / 128) * 512 : 0;
   static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
-  static constexpr int NUM_WARPS = kFp8 ? 7 : 6;
-  static constexpr int EPI_WARP0 = NUM_WARPS - 4;
+  static constexpr int EPI_WARPS = 8;                   // two per TMEM lane quarter
+  static constexpr int NUM_WARPS = (kFp8 ? 3 : 2) + EPI_WARPS;
+  static constexpr int EPI_WARP0 = NUM_WARPS - EPI_WARPS;
+  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int THREADS = NUM_WARPS * 32;
   // TMEM columns: accumulators first, then 16 columns of scale factors per stage.
   static constexpr int SF_TMEM_COL0 = ACC_BUFS * BN;
@@ -118,7 +119,13 @@ struct KCfg {
   static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
+  // epilogue staging for TMA stores: per epilogue warp, one or two 32 x 32 output blocks
+  static constexpr int OUT_BYTES = kOutF32 ? 4 : 2;
+  static constexpr int STG_BYTES = 32 * 32 * OUT_BYTES;
+  static constexpr int OFF_STG = (OFF_MISC + 16 + 1023) / 1024 * 1024;   // swizzle-atom aligned
+  static constexpr int STG_BUFS =
+      OFF_STG + EPI_WARPS * 2 * STG_BYTES + 1024 <= 232448 ? 2 : 1;
+  static constexpr int SMEM_BYTES = OFF_STG + EPI_WARPS * STG_BUFS * STG_BYTES + 1024;  // + slack
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 
   // tcgen05 instruction descriptor (kind::f16): D=f32, A=B=bf16, A K-major, B N-major.
@@ -185,21 +192,32 @@ struct UnitCoord {
   int tile, s, m_tile, n_tile, kb_begin, kb_end;
 };
 
+// Unit u -> output tile (M-fastest order) and split s; split s covers k-blocks
+// [s*q + min(s, r), (s+1)*q + min(s+1, r)) with q = KB / S, r = KB % S (fixed by K and S).
 __device__ __forceinline__ UnitCoord unit_coord(int u, const KParams& p) {
   UnitCoord c;
-  c.tile = u / p.splits;
-  c.s = u - c.tile * p.splits;
+  if (p.splits == 1) {
+    c.tile = u;
+    c.s = 0;
+    c.kb_begin = 0;
+    c.kb_end = p.kblocks;
+  } else {
+    c.tile = u / p.splits;
+    c.s = u - c.tile * p.splits;
+    const int q = p.kblocks / p.splits, r = p.kblocks - q * p.splits;
+    c.kb_begin = c.s * q + min(c.s, r);
+    c.kb_end = c.kb_begin + q + (c.s < r ? 1 : 0);
+  }
   c.m_tile = c.tile % p.m_tiles;
   c.n_tile = c.tile / p.m_tiles;
-  c.kb_begin = int((int64_t)c.s * p.kblocks / p.splits);
-  c.kb_end = int((int64_t)(c.s + 1) * p.kblocks / p.splits);
   return c;
 }
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     bi_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                   const __grid_constant__ CUtensorMap tmap_w, const KParams p) {
+                   const __grid_constant__ CUtensorMap tmap_w,
+                   const __grid_constant__ CUtensorMap tmap_y, const KParams p) {
   constexpr bool kPair = C::CTAS == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -211,7 +229,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + C::ACC_BUFS + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::ACC_BUFS);
-  const uint32_t epi_bar = drain_bar + 8u;   // split-K hand-off among the 4 epilogue warps
+  const uint32_t epi_bar = drain_bar + 8u;   // split-K hand-off among the epilogue warps
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_slot = misc + 0;
   volatile uint32_t* abort_flag = misc + 1;
@@ -224,6 +242,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const int ngroups = gridDim.x / C::CTAS;
   const int units = p.m_tiles * p.n_tiles * p.splits;
 
+  if (warp == C::EPI_WARP0) {
+    // An idle warp touches the scalar parameters first, so that their constant-cache line is
+    // resident by the time the producer computes its first tile.
+    asm volatile("" ::"r"(p.M), "r"(p.N), "r"(p.K), "r"(p.m_tiles), "r"(p.n_tiles), "r"(p.splits),
+                 "r"(p.kblocks), "r"(p.a_box_rows));
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(full_bar(s), C::kFp8 ? 2u : 1u);
@@ -231,16 +255,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     for (int b = 0; b < C::ACC_BUFS; ++b) {
       ptx::mbar_init(tfull_bar(b), 1u);
-      ptx::mbar_init(tempty_bar(b), 4u * C::CTAS);
+      ptx::mbar_init(tempty_bar(b), uint32_t(C::EPI_WARPS * C::CTAS));
     }
     ptx::mbar_init(drain_bar, 1u);
-    ptx::mbar_init(epi_bar, 4u);
+    ptx::mbar_init(epi_bar, uint32_t(C::EPI_WARPS));
     *abort_flag = 0u;
     *last_flag = 0u;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
     ptx::prefetch_tensormap(&tmap_x);
     ptx::prefetch_tensormap(&tmap_w);
+    ptx::prefetch_tensormap(&tmap_y);
   }
   if (warp == 1) {
     if constexpr (kPair) {
@@ -276,17 +301,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       bool ok = true;
       for (int u = group; u < units && ok; u += ngroups) {
         const UnitCoord uc = unit_coord(u, p);
-        const int wcol0 = uc.n_tile * C::BN + int(rank) * C::BN_CTA;
-        auto prefetch_w = [&](int kb) {
-#pragma unroll
-          for (int a = 0; a < C::N_ATOMS; ++a) ptx::tma_prefetch_2d(&tmap_w, wcol0 + a * C::ATOM_N, kb * C::BK);
-        };
-        // W k-blocks are requested into L2 ahead of the ring so that HBM stays busy when only a
-        // few CTAs stream W (small M); the hint changes no data and no arithmetic.
-        const int pf = p.prefetch_kb;
-        for (int kb = uc.kb_begin; kb < min(uc.kb_end, uc.kb_begin + pf); ++kb) prefetch_w(kb);
         for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
-          if (pf > 0 && kb + pf < uc.kb_end) prefetch_w(kb + pf);
           if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
             ok = false;
             break;
@@ -329,6 +344,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             issued_mask |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           }
+
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -504,6 +520,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if constexpr (kPair) ptx::cluster_wait();
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int epi_tid = (warp - C::EPI_WARP0) * 32 + lane;
+    // the two warps of a lane quarter split the tile's columns in halves
+    constexpr int kChunks = C::BN / 32;
+    const int half = (warp - C::EPI_WARP0) / 4;
+    const int c_begin = half * (kChunks / 2), c_end = c_begin + kChunks / 2;
+    const uint32_t stg_base =
+        sbase + C::OFF_STG + uint32_t((warp - C::EPI_WARP0) * C::STG_BUFS * C::STG_BYTES);
+    int stg_next = 0;
     int buf = 0;
     uint32_t bphase = 0, ephase = 0;
     for (int u = group; u < units; u += ngroups) {
@@ -543,17 +566,52 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
       };
       const uint32_t trow = tmem_base + uint32_t(buf * C::BN) + (uint32_t(q * 32) << 16);
+      // Unsplit tiles: each 32 x 32 block is converted into a staging buffer (row = lane) and
+      // written by one TMA store, which also clips rows >= M and columns >= N.
+      auto stage_and_store = [&](int c, const uint32_t (&r)[32]) {
+        const uint32_t dst = stg_base + uint32_t(stg_next * C::STG_BYTES);
+        if (lane == 0) ptx::bulk_wait_read<C::STG_BUFS - 1>();   // the buffer's last store has read it
+        __syncwarp();
+        // The block is laid out as the TMA store's swizzle expects (16-byte chunk j of row
+        // `lane` at chunk j ^ f(lane)), which also spreads a warp's stores over all banks.
+        if constexpr (C::kOutF32) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)                   // 128-byte rows, 128-byte swizzle
+            ptx::st_shared_v4(dst + lane * 128 + ((v ^ (lane & 7)) << 4), r[4 * v], r[4 * v + 1],
+                              r[4 * v + 2], r[4 * v + 3]);
+        } else {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {                 // 64-byte rows, 64-byte swizzle
+            const float* f = reinterpret_cast<const float*>(r + 8 * v);
+            ptx::st_shared_v4(dst + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4), ptx::pack_bf16x2(f[0], f[1]),
+                              ptx::pack_bf16x2(f[2], f[3]), ptx::pack_bf16x2(f[4], f[5]),
+                              ptx::pack_bf16x2(f[6], f[7]));
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&tmap_y, dst, col_tile0 + c * 32, row - lane);
+          ptx::bulk_commit();
+        }
+        stg_next = (stg_next + 1) % C::STG_BUFS;
+      };
       // Two 32-column TMEM loads per wait; a warp whose 32 rows all lie past M reads nothing.
 #pragma unroll 1
-      for (int c = 0; c < C::BN / 32; c += 2) {
+      for (int c = c_begin; c < c_end; c += 2) {
         if (col_tile0 + c * 32 >= p.N || !warp_has_rows) break;   // uniform across the warp
         uint32_t r0[32], r1[32];
-        const bool two = c + 1 < C::BN / 32 && col_tile0 + (c + 1) * 32 < p.N;
+        const bool two = c + 1 < c_end && col_tile0 + (c + 1) * 32 < p.N;
         ptx::tmem_ld_32x32b_x32(trow + uint32_t(c * 32), r0);
         if (two) ptx::tmem_ld_32x32b_x32(trow + uint32_t((c + 1) * 32), r1);
         ptx::tmem_wait_ld();
-        store_chunk(c, r0);
-        if (two) store_chunk(c + 1, r1);
+        if (p.splits > 1) {
+          store_chunk(c, r0);
+          if (two) store_chunk(c + 1, r1);
+        } else {
+          stage_and_store(c, r0);
+          if (two) stage_and_store(c + 1, r1);
+        }
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -591,7 +649,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const float* src0 = p.ws + (((size_t)sub * p.splits) * kBM + row_in_tile) * C::BN;
             const size_t sstride = (size_t)kBM * C::BN;
 #pragma unroll 1
-            for (int c = 0; c < C::BN / 32; ++c) {
+            for (int c = c_begin; c < c_end; ++c) {
               const int col0 = col_tile0 + c * 32;
               if (col0 >= p.N) break;
               const int nvalid = min(32, p.N - col0);
@@ -632,6 +690,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   }
 
+  if (warp >= C::EPI_WARP0 && lane == 0) ptx::bulk_wait_all();   // output stores complete
   ptx::tc_fence_before();
   __syncthreads();
   if constexpr (kPair) ptx::cluster_sync();   // neither CTA leaves while the pair still works

@@ -72,12 +72,12 @@ def test_null_arguments():
     assert L.bi_gemm_get_config(None, None) == bg.BI_GEMM_ERR_INVALID_ARG
     b = ctypes.c_uint64()
     assert L.bi_gemm_workspace_size(None, 4, ctypes.byref(b)) == bg.BI_GEMM_ERR_INVALID_ARG
-    opts = bg.bi_gemm_options(-1, 0, 0, 0)
+    opts = bg.bi_gemm_options(-1, 0, 0)
     h = ctypes.c_void_p()
     assert L.bi_gemm_create_ex(ctypes.byref(h), 256, 128, 0, 0, ctypes.byref(opts)) == bg.BI_GEMM_ERR_INVALID_ARG
-    opts = bg.bi_gemm_options(5, 0, 0, 0)   # 5 > ceil(256 / 64) k-blocks
+    opts = bg.bi_gemm_options(5, 0, 0)   # 5 > ceil(256 / 64) k-blocks
     assert L.bi_gemm_create_ex(ctypes.byref(h), 256, 128, 0, 0, ctypes.byref(opts)) == bg.BI_GEMM_ERR_INVALID_ARG
-    opts = bg.bi_gemm_options(0, 0, 0, -2)   # prefetch distance out of range
+    opts = bg.bi_gemm_options(0, -3, 0)   # negative grid bound
     assert L.bi_gemm_create_ex(ctypes.byref(h), 256, 128, 0, 0, ctypes.byref(opts)) == bg.BI_GEMM_ERR_INVALID_ARG
 
 
