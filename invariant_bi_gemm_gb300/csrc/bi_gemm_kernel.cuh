@@ -284,10 +284,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const SyncCtx sc{abort_flag, p.status, p.timeout_ns};
-  // Everything above touched only this CTA's shared memory and TMEM, so it may overlap the
-  // tail of the previous kernel in the stream; global memory is read or written only after
-  // that kernel has completed.
-  ptx::grid_dependency_wait();
+  // Set-up touches only this CTA's shared memory and TMEM, so it may overlap the tail of the
+  // previous kernel in the stream.  Each role waits for that kernel to complete
+  // (grid_dependency_wait) just before its first global-memory access.
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -298,13 +297,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_par = 0;   // per stage: an issue is outstanding / its parity
-      bool ok = true;
+      bool ok = true, dep_done = false;
       for (int u = group; u < units && ok; u += ngroups) {
         const UnitCoord uc = unit_coord(u, p);
         for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
           if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
             ok = false;
             break;
+          }
+          if (!dep_done) {
+            ptx::grid_dependency_wait();
+            dep_done = true;
           }
           bool skip = false;
 #ifdef BI_GEMM_CONTROLS
@@ -472,6 +475,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t phase = 0;
     const int KB32 = p.K / 32;
     bool ok = true;
+    ptx::grid_dependency_wait();
     for (int u = group; u < units && ok; u += ngroups) {
       const UnitCoord uc = unit_coord(u, p);
       for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
@@ -529,6 +533,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int stg_next = 0;
     int buf = 0;
     uint32_t bphase = 0, ephase = 0;
+    ptx::grid_dependency_wait();
     for (int u = group; u < units; u += ngroups) {
       const UnitCoord uc = unit_coord(u, p);
       if (!warp_wait_phase(tfull_bar(buf), bphase, sc, kErrTimeoutEpilogue)) break;
@@ -690,7 +695,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
   }
 
-  if (warp >= C::EPI_WARP0 && lane == 0) ptx::bulk_wait_all();   // output stores complete
+  // the output stores must have read their staging buffers before shared memory is released
+  if (warp >= C::EPI_WARP0 && lane == 0) ptx::bulk_wait_read<0>();
   ptx::tc_fence_before();
   __syncthreads();
   if constexpr (kPair) ptx::cluster_sync();   // neither CTA leaves while the pair still works
