@@ -34,6 +34,12 @@ namespace bigemm {
 
 constexpr int kVersion = (1 << 16) | 0;
 constexpr uint64_t kDefaultTimeoutNs = 5ull * 1000 * 1000 * 1000;
+// Raster order (visiting order only; it decides no arithmetic): while x fits comfortably in L2
+// the M tiles vary fastest (x stays resident, W streams once); a larger x is visited in groups
+// of 16 N tiles, so that the W slabs of a group (16 x K x 256 x 2 bytes) stay resident while x
+// is re-read once per group.
+constexpr int64_t kRasterXResidentBytes = int64_t(40) << 20;
+constexpr int64_t kRasterGroupN = 16;
 
 // ------------------------------------------------------------------ kernel table
 
@@ -282,6 +288,8 @@ int launch_core(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_ge
   p.splits = split;
   p.kblocks = h->kblocks;
   p.a_box_rows = int32_t(a_box_rows);
+  const int64_t x_bytes = M * h->K * (fp8 ? 1 : 2);
+  p.group_n = int32_t(x_bytes <= kRasterXResidentBytes ? 1 : std::min<int64_t>(kRasterGroupN, h->n_tiles));
   p.timeout_ns = h->timeout_ns;
   p.test_flags = test_flags;
 

@@ -63,6 +63,7 @@ struct KParams {
   int32_t splits;           // S
   int32_t kblocks;          // KB = ceil(K / BK)
   int32_t a_box_rows;       // rows per x TMA box: 128, or round_up(M, 8) when M < 128
+  int32_t group_n;          // raster order: N tiles per group (M tiles vary fastest within it)
   uint64_t timeout_ns;
   uint32_t test_flags;      // only read by the control build
 };
@@ -192,8 +193,11 @@ struct UnitCoord {
   int tile, s, m_tile, n_tile, kb_begin, kb_end;
 };
 
-// Unit u -> output tile (M-fastest order) and split s; split s covers k-blocks
-// [s*q + min(s, r), (s+1)*q + min(s+1, r)) with q = KB / S, r = KB % S (fixed by K and S).
+// Unit u -> output tile and split s.  Tiles are visited in groups of group_n N-tiles; within a
+// group the N tile varies fastest and the M tile slowest, so the tiles resident at one time
+// share a few x row blocks and a few W column slabs (L2 reuse).  The order decides no
+// arithmetic.  Split s covers k-blocks [s*q + min(s, r), (s+1)*q + min(s+1, r)) with
+// q = KB / S, r = KB % S (fixed by K and S).
 __device__ __forceinline__ UnitCoord unit_coord(int u, const KParams& p) {
   UnitCoord c;
   if (p.splits == 1) {
@@ -208,8 +212,12 @@ __device__ __forceinline__ UnitCoord unit_coord(int u, const KParams& p) {
     c.kb_begin = c.s * q + min(c.s, r);
     c.kb_end = c.kb_begin + q + (c.s < r ? 1 : 0);
   }
-  c.m_tile = c.tile % p.m_tiles;
-  c.n_tile = c.tile / p.m_tiles;
+  const int per_group = p.group_n * p.m_tiles;
+  const int g = c.tile / per_group;
+  const int local = c.tile - g * per_group;
+  const int gn = min(p.group_n, p.n_tiles - g * p.group_n);   // N tiles in this (last) group
+  c.m_tile = local / gn;
+  c.n_tile = g * p.group_n + (local - c.m_tile * gn);
   return c;
 }
 
@@ -649,39 +657,44 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ephase ^= 1u;
         const bool last = *last_flag != 0u;
         if (last) {
+          // The (row, 4-column group) items of this 128-row sub-tile are spread over all epilogue
+          // threads; each item sums its S partials strictly in split order,
+          // ((p0 + p1) + p2) + ..., with the loads issued in independent batches of 16.
           __threadfence();
-          if (row < p.M) {
-            const float* src0 = p.ws + (((size_t)sub * p.splits) * kBM + row_in_tile) * C::BN;
-            const size_t sstride = (size_t)kBM * C::BN;
+          const int row0 = uc.m_tile * C::TILE_M + int(rank) * kBM;
+          const int rows = min(kBM, p.M - row0);
+          const int groups = (min(C::BN, p.N - col_tile0) + 3) / 4;
+          const float* src0 = p.ws + ((size_t)sub * p.splits) * kBM * C::BN;
+          const size_t sstride = (size_t)kBM * C::BN;
 #pragma unroll 1
-            for (int c = c_begin; c < c_end; ++c) {
-              const int col0 = col_tile0 + c * 32;
-              if (col0 >= p.N) break;
-              const int nvalid = min(32, p.N - col0);
+          for (int it = epi_tid; it < rows * groups; it += C::EPI_THREADS) {
+            const int rr = it / groups, g4 = it - rr * groups;
+            const float* sp = src0 + (size_t)rr * C::BN + g4 * 4;
+            float4 acc = __ldcg(reinterpret_cast<const float4*>(sp));
 #pragma unroll 1
-              for (int v = 0; v < 8; ++v) {
-                if (v * 4 >= nvalid) break;
-                const float* sp = src0 + c * 32 + v * 4;
-                float4 acc = __ldcg(reinterpret_cast<const float4*>(sp));
-#pragma unroll 1
-                for (int s = 1; s < p.splits; ++s) {
-                  const float4 t = __ldcg(reinterpret_cast<const float4*>(sp + s * sstride));
-                  acc.x = acc.x + t.x;
-                  acc.y = acc.y + t.y;
-                  acc.z = acc.z + t.z;
-                  acc.w = acc.w + t.w;
-                }
-                if constexpr (C::kOutF32) {
-                  float* dst = reinterpret_cast<float*>(p.y) + (size_t)row * p.N + col0 + v * 4;
-                  *reinterpret_cast<float4*>(dst) = acc;
-                } else {
-                  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)row * p.N + col0 + v * 4;
-                  uint2 pk;
-                  pk.x = ptx::pack_bf16x2(acc.x, acc.y);
-                  pk.y = ptx::pack_bf16x2(acc.z, acc.w);
-                  *reinterpret_cast<uint2*>(dst) = pk;
+            for (int s0 = 1; s0 < p.splits; s0 += 16) {
+              float4 t[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (s0 + j < p.splits) t[j] = __ldcg(reinterpret_cast<const float4*>(sp + (s0 + j) * sstride));
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (s0 + j < p.splits) {
+                  acc.x = acc.x + t[j].x;
+                  acc.y = acc.y + t[j].y;
+                  acc.z = acc.z + t[j].z;
+                  acc.w = acc.w + t[j].w;
                 }
               }
+            }
+            const size_t yo = (size_t)(row0 + rr) * p.N + col_tile0 + g4 * 4;
+            if constexpr (C::kOutF32) {
+              *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + yo) = acc;
+            } else {
+              uint2 pk;
+              pk.x = ptx::pack_bf16x2(acc.x, acc.y);
+              pk.y = ptx::pack_bf16x2(acc.z, acc.w);
+              *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.y) + yo) = pk;
             }
           }
           if (epi_tid == 0) p.counters[sub] = 0u;   // ready for the next launch
