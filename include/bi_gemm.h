@@ -59,8 +59,8 @@ typedef enum {
 
 /* Device pointers to the two scale matrices (MXFP8 only). */
 typedef struct {
-  const uint8_t* sx; /* [M, K/32] E8M0, 4-byte aligned */
-  const uint8_t* sw; /* [K/32, N] E8M0                 */
+  const uint8_t* sx; /* [M, K/32] E8M0, 4-byte aligned (else BI_GEMM_ERR_ALIGNMENT) */
+  const uint8_t* sw; /* [K/32, N] E8M0, 16-byte aligned (else BI_GEMM_ERR_ALIGNMENT) */
 } bi_gemm_scales;
 
 enum {
@@ -124,8 +124,9 @@ int bi_gemm_run(bi_gemm_t h, const void* x, int64_t M, const void* W,
  *     with that device current) and remembers it; make that first call before any stream
  *     capture.  The handle's device must be current (else BI_GEMM_ERR_INVALID_ARG).
  *   - A run whose scratch would not fit returns BI_GEMM_ERR_SCRATCH_LIMIT and queues nothing:
- *     tiles = ceil(M/128) * ceil(N/BN) must be <= 1024 and tiles*S*128*BN*4 bytes must be
- *     <= 8 MiB - 4 KiB (bi_gemm_get_config gives S and BN).  Handles with S == 1 use no scratch.
+ *     the 128-row sub-tiles, tiles = ceil(M/block_m) * ctas_per_tile * ceil(N/BN), must be
+ *     <= 1024 and tiles*S*128*BN*4 bytes must be <= 8 MiB - 4 KiB (bi_gemm_get_config gives
+ *     block_m, ctas_per_tile, S and BN).  Handles with S == 1 use no scratch.
  *   - All calls in the process share the one array per device and it keeps the last call's
  *     contents; each call first clears, on `stream`, the counters it uses.  Calls whose work
  *     overlaps on the GPU (other streams, other threads, other handles) race on the array and

@@ -4,8 +4,8 @@
 // The configuration rule ("Batch-invariant matrix multiplication", nondeterminism article:
 // compile one kernel configuration and use it for all shapes; strategy switches keyed on
 // the block/SM ratio are where libraries lose invariance):
-//   tile      128 x BN, BN = 64 / 128 / 256 (bf16) or 128 / 256 (MXFP8) from N alone; for
-//             bf16 with BN = 256 the tile is 256 x 256 on a CTA pair (cta_group::2);
+//   tile      128 x BN, BN = 64 / 128 / 256 (bf16) or 128 / 256 (MXFP8) from N alone; with
+//             BN = 256 the tile is 256 x 256 on a CTA pair (cta_group::2);
 //   MMA       tcgen05.mma M=128 (M=256 on a pair), N=BN, K=16 (bf16) or K=32 (MXFP8);
 //   K stage   128 bytes of K per stage (64 bf16 / 128 E4M3), ascending k-blocks;
 //   split S   1, except for a single N tile (N <= BN) with a long K, where
@@ -70,6 +70,11 @@ KernelInfo info_of() {
 #ifndef BI_GEMM_PAIR_STAGES
 #define BI_GEMM_PAIR_STAGES 6
 #endif
+// Pipeline depth of the MXFP8 pair tile (a stage: 16 KB of x, 16 KB of W and 1.5 KB of scales
+// per CTA; one accumulator, since 256 fp32 columns plus the scale columns fill the TMEM).
+#ifndef BI_GEMM_FP8_PAIR_STAGES
+#define BI_GEMM_FP8_PAIR_STAGES 6
+#endif
 
 // dtype 0/1: bf16 in, bf16/f32 out; dtype 2: MXFP8 in, bf16 out.
 static KernelInfo select_kernel(int dtype, int bn) {
@@ -84,7 +89,7 @@ static KernelInfo select_kernel(int dtype, int bn) {
       return info_of<KCfg<false, true, 256, BI_GEMM_PAIR_STAGES, 2, 2>>();
     default:
       if (bn == 128) return info_of<KCfg<true, false, 128, 6, 2>>();
-      return info_of<KCfg<true, false, 256, 4, 1>>();
+      return info_of<KCfg<true, false, 256, BI_GEMM_FP8_PAIR_STAGES, 1, 2>>();
   }
 }
 
@@ -346,7 +351,7 @@ int validate_run(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_g
   if (!is_aligned(x, 16) || !is_aligned(W, 16) || !is_aligned(y, 16)) return BI_GEMM_ERR_ALIGNMENT;
   if (h->dtype == BI_MXFP8E4M3_OUT_BF16) {
     if (!scales || !scales->sx || !scales->sw) return BI_GEMM_ERR_INVALID_ARG;
-    if (!is_aligned(scales->sx, 4)) return BI_GEMM_ERR_ALIGNMENT;
+    if (!is_aligned(scales->sx, 4) || !is_aligned(scales->sw, 16)) return BI_GEMM_ERR_ALIGNMENT;
   } else if (scales && (scales->sx || scales->sw)) {
     return BI_GEMM_ERR_INVALID_ARG;
   }

@@ -20,15 +20,18 @@
 //
 // Tile = 128 x BN per CTA, or 256 x BN per CTA pair (CTAS = 2, BN = 256): the pair issues one
 // tcgen05.mma.cta_group::2 of M=256, each CTA staging its own 128 rows of x and its own BN/2
-// columns of W and receiving its 128 rows of the accumulator in its own TMEM.  The pair is one
-// fixed configuration chosen from N, like everything else.
+// columns of W and receiving its 128 rows of the accumulator in its own TMEM.  For MXFP8 each
+// CTA also stages its own rows' x scales and the scales of all BN columns of W, which the
+// block-scaled pair MMA reads from each CTA's own TMEM.  The pair is one fixed configuration
+// chosen from N, like everything else.
 //
 // Warp roles (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer: x tile [128 x BK] (K-major, 128-byte swizzle) and W tile
 //               [BK x BN] (N-major, 128-byte swizzle) per pipeline stage;
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
-//   warp 2      (MXFP8 only) scale producer: E8M0 scales into the tcgen05.cp layout;
-//   last 4      epilogue: tcgen05.ld -> round to nearest even -> 16-byte global stores,
+//   warps 2-3   (MXFP8 only) scale producers, taking the k-blocks in turn: E8M0 scales into
+//               the tcgen05.cp layout;
+//   last 8      epilogue: tcgen05.ld -> round to nearest even -> TMA stores of 32 x 32 blocks,
 //               or fp32 partials + ordered merge when S > 1.
 // Every wait is bounded in time; on expiry the kernel records an error bit in the
 // handle's status word, lets in-flight copies and MMAs finish, frees TMEM and returns.
@@ -82,8 +85,8 @@ struct KCfg {
   static constexpr int STAGES = kStages_;
   static constexpr int ACC_BUFS = kAccBufs_;
   static constexpr int CTAS = kCtas_;                   // CTAs per output tile (1 or 2)
-  static_assert(CTAS == 1 || (CTAS == 2 && !kFp8_ && (kBN_ == 256 || kBN_ == 192)),
-                "CTA pairs: bf16, BN = 256 or 192");
+  static_assert(CTAS == 1 || (CTAS == 2 && (kBN_ == 256 || (!kFp8_ && kBN_ == 192))),
+                "CTA pairs: BN = 256 (bf16 or MXFP8) or 192 (bf16)");
   static constexpr int TILE_M = kBM * CTAS;
   static constexpr int BN_CTA = BN / CTAS;              // W columns staged by each CTA
   static constexpr int ELEM = kFp8 ? 1 : 2;
@@ -101,10 +104,15 @@ struct KCfg {
   static constexpr int B_ATOM_BYTES = BK * B_SW;
   static constexpr int B_BYTES = N_ATOMS * B_ATOM_BYTES;
   static constexpr int SFA_BYTES = kFp8 ? 512 : 0;      // 128 rows x 4 k-blocks
+  // Each CTA stages the scales of all BN columns: on a pair, the block-scaled MMA reads the B
+  // scales of the whole N extent from each CTA's own TMEM.
   static constexpr int SFB_BYTES = kFp8 ? (BN / 128) * 512 : 0;
   static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
   static constexpr int EPI_WARPS = 8;                   // two per TMEM lane quarter
-  static constexpr int NUM_WARPS = (kFp8 ? 3 : 2) + EPI_WARPS;
+  // MXFP8: scale-producer warps take the k-blocks in turn, so that the global-load latency of
+  // several stages' scales overlaps.
+  static constexpr int SCALE_WARPS = kFp8 ? 2 : 0;
+  static constexpr int NUM_WARPS = 2 + SCALE_WARPS + EPI_WARPS;
   static constexpr int EPI_WARP0 = NUM_WARPS - EPI_WARPS;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int THREADS = NUM_WARPS * 32;
@@ -117,8 +125,12 @@ struct KCfg {
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 2;
+  // MXFP8: per scale warp, two prefetch buffers of one k-block's scales each
+  static constexpr int OFF_SFRAW = OFF_SF + STAGES * SF_BYTES;
+  static constexpr int OFF_BAR = OFF_SFRAW + SCALE_WARPS * 2 * SF_BYTES;
+  // full, empty, accumulator full / empty, drain, epilogue; MXFP8 adds per stage the peer's
+  // scales-ready barrier and per scale warp a drain barrier for its scale copies
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 2 + (kFp8 ? STAGES + SCALE_WARPS : 0);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   // epilogue staging for TMA stores: per epilogue warp, one or two 32 x 32 output blocks
   static constexpr int OUT_BYTES = kOutF32 ? 4 : 2;
@@ -137,7 +149,7 @@ struct KCfg {
   // B N-major, E8M0 scales; the scale-factor byte selectors are OR-ed in per K step.
   static constexpr uint32_t IDESC_MXF8 =
       (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) | (uint32_t(BN >> 3) << 17) |
-      (1u << 23) | (uint32_t(kBM >> 4) << 24);
+      (1u << 23) | (uint32_t(TILE_M >> 4) << 24);
 };
 
 // Shared-memory matrix descriptor: start, leading / stride byte offsets, version 1, layout.
@@ -157,12 +169,29 @@ struct SyncCtx {
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the abort flag and the error
 // bit) once the time limit passes, or as soon as another role has aborted.
+// How a wait observes a barrier phase: acquire at CTA scope (default), acquire at cluster scope
+// (the phase completes with arrivals from the peer CTA), or relaxed (nothing is ordered around
+// the test, so loads the waiting thread has in flight stay in flight; the writes that follow a
+// relaxed wait depend on its outcome by control only).
+enum class Wait { kCta, kCluster, kRelaxed };
+
+template <Wait kW = Wait::kCta>
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
+  if constexpr (kW == Wait::kCluster)
+    return ptx::mbar_try_wait_cluster(bar, parity);
+  else if constexpr (kW == Wait::kRelaxed)
+    return ptx::mbar_try_wait_relaxed(bar, parity);
+  else
+    return ptx::mbar_try_wait(bar, parity);
+}
+
+template <Wait kW = Wait::kCta>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const SyncCtx& c,
                                            uint32_t err_bit) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (try_wait<kW>(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (try_wait<kW>(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*c.abort) return false;
       if (ptx::globaltimer() - t0 > c.timeout_ns) {
@@ -176,14 +205,15 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, and on success every
 // lane observes the (already completed) phase itself before touching the guarded data.
+template <Wait kW = Wait::kCta>
 __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, const SyncCtx& c,
                                                 uint32_t err_bit) {
   const int lane = threadIdx.x & 31;
   uint32_t ok = 1;
-  if (lane == 0) ok = wait_phase(bar, parity, c, err_bit) ? 1u : 0u;
+  if (lane == 0) ok = wait_phase<kW>(bar, parity, c, err_bit) ? 1u : 0u;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (ok) {
-    for (int i = 0; i < (1 << 20) && !ptx::mbar_try_wait(bar, parity); ++i) {
+    for (int i = 0; i < (1 << 20) && !try_wait<kW>(bar, parity); ++i) {
     }
   }
   return ok != 0;
@@ -238,6 +268,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + C::ACC_BUFS + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::ACC_BUFS);
   const uint32_t epi_bar = drain_bar + 8u;   // split-K hand-off among the epilogue warps
+  // MXFP8: the peer CTA's scales for a stage are in its shared memory (pairs only)
+  auto sfpeer_bar = [&](int s) { return epi_bar + 8u + 8u * s; };
+  // MXFP8: completion of a scale warp's last scale copies
+  auto sfdrain_bar = [&](int w) { return epi_bar + 8u + 8u * (C::STAGES + w); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_slot = misc + 0;
   volatile uint32_t* abort_flag = misc + 1;
@@ -258,6 +292,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
+      // TMA bytes (+ the commit of the stage's scale copies, MXFP8)
       ptx::mbar_init(full_bar(s), C::kFp8 ? 2u : 1u);
       ptx::mbar_init(empty_bar(s), 1u);
     }
@@ -267,6 +302,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     ptx::mbar_init(drain_bar, 1u);
     ptx::mbar_init(epi_bar, uint32_t(C::EPI_WARPS));
+    if constexpr (C::kFp8) {
+      for (int s = 0; s < C::STAGES; ++s) ptx::mbar_init(sfpeer_bar(s), 1u);
+      for (int w = 0; w < C::SCALE_WARPS; ++w) ptx::mbar_init(sfdrain_bar(w), 1u);
+    }
     *abort_flag = 0u;
     *last_flag = 0u;
     ptx::fence_barrier_init();
@@ -410,22 +449,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const uint32_t a_addr = sbase + C::OFF_A + stage * C::A_BYTES;
           const uint32_t b_addr = sbase + C::OFF_B + stage * C::B_BYTES;
           if constexpr (C::kFp8) {
-            const uint32_t sf_addr = sbase + C::OFF_SF + stage * C::SF_BYTES;
+            // the stage's scales are already in TMEM: their copies were committed to full_bar
             const uint32_t sfa_t = tmem_base + uint32_t(C::SF_TMEM_COL0 + 16 * stage);
             const uint32_t sfb_t = sfa_t + 8u;
-            ptx::tc_cp_32x128b_x4(sfa_t, make_sdesc(sf_addr, 0, 128, kLayoutNone));
-#pragma unroll
-            for (int b = 0; b < C::BN / 128; ++b)
-              ptx::tc_cp_32x128b_x4(sfb_t + 4u * b,
-                                    make_sdesc(sf_addr + C::SFA_BYTES + 512 * b, 0, 128, kLayoutNone));
 #pragma unroll
             for (int kk = 0; kk < C::K_STEPS; ++kk) {
               const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
               const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
                                              8 * C::B_SW, C::B_LAYOUT);
               const uint32_t idesc = C::IDESC_MXF8 | (uint32_t(kk) << 4) | (uint32_t(kk) << 29);
-              ptx::mma_mxf8(d_tmem, ad, bd, idesc, sfa_t, sfb_t,
-                            (kb != uc.kb_begin || kk != 0) ? 1u : 0u);
+              const uint32_t acc = (kb != uc.kb_begin || kk != 0) ? 1u : 0u;
+              if constexpr (kPair)
+                ptx::mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
+              else
+                ptx::mma_mxf8(d_tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
             }
           } else {
 #pragma unroll
@@ -473,57 +510,169 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (C::kFp8 && warp == 2) {
-    // ------------------------------------------------------------ scale producer (MXFP8)
-    if constexpr (kPair) ptx::cluster_wait();
-    // Layout expected by tcgen05.cp 32x128b.warpx4 for 128 rows x 4 k-blocks (512 bytes):
-    // byte (r % 32) * 16 + (r / 32) * 4 + kblk.  One 512-byte block for x's rows, one per
-    // 128 columns of W.
-    int stage = 0;
-    uint32_t phase = 0;
-    const int KB32 = p.K / 32;
-    bool ok = true;
-    ptx::grid_dependency_wait();
-    for (int u = group; u < units && ok; u += ngroups) {
-      const UnitCoord uc = unit_coord(u, p);
-      for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
-        if (!warp_wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutScales)) {
-          ok = false;
-          break;
+  } else if (C::kFp8 && warp < 2 + C::SCALE_WARPS) {
+    if constexpr (C::kFp8) {
+      // ---------------------------------------------------------- scale producers (MXFP8)
+      if constexpr (kPair) ptx::cluster_wait();
+      // Layout expected by tcgen05.cp 32x128b.warpx4 for 128 rows x 4 k-blocks (512 bytes):
+      // byte (r % 32) * 16 + (r / 32) * 4 + kblk.  One 512-byte block for this CTA's 128 rows
+      // of x, one per 128 columns of the tile's W columns (all BN of them, on a pair too).
+      // This CTA's k-block items are numbered it = 0, 1, ... in pipeline order; scale warp j
+      // fills items j, j + SCALE_WARPS, ...  While it waits for an item's stage, a warp already
+      // has its next item's scales on the way into shared memory (cp.async).
+      // On a pair the peer's warp publishes its stage to the leader (sfpeer_bar); the leader's
+      // warp then issues the tcgen05.cp of both CTAs' scales and commits them to the stage's
+      // full barrier, so the MMA issuer finds the scales in TMEM and issues only MMAs.
+      const int sw_id = warp - 2;
+      const int KB32 = p.K / 32;
+      int u = group, kb = 0, kb_end = 0, row_base = 0, col_base = 0;
+      auto enter_unit = [&]() {
+        const UnitCoord uc = unit_coord(u, p);
+        kb = uc.kb_begin;
+        kb_end = uc.kb_end;
+        row_base = uc.m_tile * C::TILE_M + int(rank) * kBM;
+        col_base = uc.n_tile * C::BN;
+      };
+      // step to the next item; false once this CTA has none left
+      auto advance = [&]() -> bool {
+        ++kb;
+        while (kb >= kb_end) {
+          u += ngroups;
+          if (u >= units) return false;
+          enter_unit();
         }
-        const uint32_t sf_addr = sbase + C::OFF_SF + stage * C::SF_BYTES;
-        uint32_t wa[4];
+        return true;
+      };
+      // Prefetch buffer: [x scales, 512 B, already in the tcgen05.cp layout | W scales as stored:
+      // 4 rows x BN bytes].  Filled by cp.async, so the warp never waits on the loads in flight.
+      const uint32_t raw0 = sbase + C::OFF_SFRAW + uint32_t(sw_id * 2 * C::SF_BYTES);
+      constexpr int kChunksPerRow = C::BN / 16;                   // 16-byte chunks per W scale row
+      auto load = [&](uint32_t raw) {
+        // x: this k-block's four scales of a row (one 32-bit word) go straight to the row's place
+        // in the layout; rows at or past M are zero-filled (their outputs are never stored)
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const int row = uc.m_tile * kBM + g * 32 + lane;
-          wa[g] = row < p.M ? __ldg(reinterpret_cast<const uint32_t*>(p.sx + (size_t)row * KB32) + kb)
-                            : 0x7F7F7F7Fu;
+          const int r = g * 32 + lane;
+          const int row = row_base + r;
+          const bool in = row < p.M;
+          ptx::cp_async_4(raw + uint32_t((r & 31) * 16 + (r >> 5) * 4),
+                          in ? p.sx + (size_t)row * KB32 + 4 * kb : p.sx, in ? 4u : 0u);
         }
-        ptx::st_shared_v4(sf_addr + lane * 16, wa[0], wa[1], wa[2], wa[3]);
+        // W: the four scale rows of this k-block over the tile's BN columns, in 16-byte chunks;
+        // columns at or past N (whole chunks, N % 16 == 0) are zero-filled (never stored)
+#pragma unroll
+        for (int i = 0; i < C::BN / 128; ++i) {
+          const int c = i * 32 + lane;
+          const int t = c / kChunksPerRow, cc = c - t * kChunksPerRow;
+          const int col = col_base + cc * 16;
+          const bool in = col < p.N;
+          ptx::cp_async_16(raw + uint32_t(C::SFA_BYTES + t * C::BN + cc * 16),
+                           in ? p.sw + (size_t)(kb * 4 + t) * p.N + col : p.sw, in ? 16u : 0u);
+        }
+        ptx::cp_async_commit();
+      };
+      ptx::grid_dependency_wait();
+      bool ok = true, copied = false;   // lane 0: no wait gave up / issued scale copies
+      bool valid = u < units;
+      if (valid) enter_unit();
+      for (int i = 0; i < sw_id && valid; ++i) valid = advance();
+      int it = sw_id;
+      uint32_t buf = 0;
+      if (valid) load(raw0);
+      while (valid) {
+        const int stage = it % C::STAGES;
+        const uint32_t phase = uint32_t(it / C::STAGES) & 1u;
+        const uint32_t raw = raw0 + buf * C::SF_BYTES;
+        // prefetch this warp's next k-block into the other buffer (its data was consumed last time)
+        bool next = true;
+        for (int i = 0; i < C::SCALE_WARPS && next; ++i) next = advance();
+        if (next) load(raw0 + (buf ^ 1u) * C::SF_BYTES);
+        if (!warp_wait_phase<Wait::kRelaxed>(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutScales)) break;
+        if (next)
+          ptx::cp_async_wait<1>();       // this k-block's copies have landed
+        else
+          ptx::cp_async_wait<0>();
+        __syncwarp();                    // ... for every lane's copies
+        const uint32_t sf_addr = sbase + C::OFF_SF + stage * C::SF_BYTES;
+        {
+          uint32_t a0, a1, a2, a3;
+          ptx::ld_shared_v4(raw + lane * 16, a0, a1, a2, a3);
+          ptx::st_shared_v4(sf_addr + lane * 16, a0, a1, a2, a3);
+        }
 #pragma unroll
         for (int b = 0; b < C::BN / 128; ++b) {
-          uint32_t wb[4];
+          // lane l takes columns 4l .. 4l+3 of each scale row; a 4 x 4 byte transpose gives v[j],
+          // the four k-block scales of column 4l + j
+          uint32_t w[4];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int col = uc.n_tile * C::BN + b * 128 + g * 32 + lane;
-            uint32_t v = 0x7F7F7F7Fu;
-            if (col < p.N) {
-              v = 0;
+          for (int t = 0; t < 4; ++t) w[t] = ptx::ld_shared_u32(raw + C::SFA_BYTES + t * C::BN + b * 128 + 4 * lane);
+          const uint32_t lo01 = __byte_perm(w[0], w[1], 0x5140);
+          const uint32_t hi01 = __byte_perm(w[0], w[1], 0x7362);
+          const uint32_t lo23 = __byte_perm(w[2], w[3], 0x5140);
+          const uint32_t hi23 = __byte_perm(w[2], w[3], 0x7362);
+          const uint32_t v[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                                 __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+          const uint32_t blk = sf_addr + C::SFA_BYTES + b * 512;
 #pragma unroll
-              for (int t = 0; t < 4; ++t)
-                v |= uint32_t(__ldg(p.sw + (size_t)(kb * 4 + t) * p.N + col)) << (8 * t);
-            }
-            wb[g] = v;
+          for (int j = 0; j < 4; ++j) {
+            const int c = 4 * lane + j;                    // column within this 128-column block
+            ptx::st_shared_u32(blk + (c & 31) * 16 + (c >> 5) * 4, v[j]);
           }
-          ptx::st_shared_v4(sf_addr + C::SFA_BYTES + b * 512 + lane * 16, wb[0], wb[1], wb[2], wb[3]);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(full_bar(stage));
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
+        if (lane == 0) {
+          if (kPair && rank != 0) {
+            // peer: publish this stage's scales to the leader, which copies them into TMEM
+            ptx::fence_release_shared();
+            ptx::mbar_arrive_remote_relaxed(ptx::mapa_shared(sfpeer_bar(stage), 0));
+          } else {
+            // leader (or single CTA): once the peer's scales are in place too, copy both CTAs'
+            // scales into TMEM and count the copies' completion on the stage's full barrier
+            bool ready = true;
+            if constexpr (kPair) ready = wait_phase<Wait::kCluster>(sfpeer_bar(stage), phase, sc, kErrTimeoutScales);
+            if (ready) {
+              ptx::tc_fence_after();
+              const uint32_t sfa_t = tmem_base + uint32_t(C::SF_TMEM_COL0 + 16 * stage);
+              const uint32_t sfb_t = sfa_t + 8u;
+              const uint64_t sfa_d = make_sdesc(sf_addr, 0, 128, kLayoutNone);
+              if constexpr (kPair)
+                ptx::tc_cp_32x128b_x4_pair(sfa_t, sfa_d);
+              else
+                ptx::tc_cp_32x128b_x4(sfa_t, sfa_d);
+#pragma unroll
+              for (int b = 0; b < C::BN / 128; ++b) {
+                const uint64_t sfb_d = make_sdesc(sf_addr + C::SFA_BYTES + 512 * b, 0, 128, kLayoutNone);
+                if constexpr (kPair)
+                  ptx::tc_cp_32x128b_x4_pair(sfb_t + 4u * b, sfb_d);
+                else
+                  ptx::tc_cp_32x128b_x4(sfb_t + 4u * b, sfb_d);
+              }
+              if constexpr (kPair)
+                ptx::tc_commit_pair_mc(full_bar(stage), 0x1);
+              else
+                ptx::tc_commit(full_bar(stage));
+              copied = true;
+            }
+            ok = ready;
+          }
         }
+        if (!__shfl_sync(0xffffffffu, ok ? 1u : 0u, 0)) break;
+        it += C::SCALE_WARPS;
+        buf ^= 1u;
+        valid = next;
+      }
+      ptx::cp_async_wait<0>();   // no copy may still target shared memory when the CTA exits
+      // the last scale copies must land before the CTA may release TMEM
+      if (lane == 0 && copied) {
+        if constexpr (kPair)
+          ptx::tc_commit_pair_mc(sfdrain_bar(sw_id), 0x1);
+        else
+          ptx::tc_commit(sfdrain_bar(sw_id));
+        SyncCtx drain{abort_flag, p.status, p.timeout_ns};
+        volatile uint32_t no_abort = 0;
+        drain.abort = &no_abort;
+        wait_phase(sfdrain_bar(sw_id), 0u, drain, kErrTimeoutScales);
       }
     }
     __syncwarp();
@@ -609,7 +758,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         stg_next = (stg_next + 1) % C::STG_BUFS;
       };
+      // Tell the MMA issuer this warp has read its part of the accumulator.
+      auto release_accumulator = [&]() {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair) {
+            ptx::fence_release_shared();
+            ptx::mbar_arrive_remote_relaxed(ptx::mapa_shared(tempty_bar(buf), 0));   // the leader's
+          } else {
+            ptx::mbar_arrive(tempty_bar(buf));
+          }
+        }
+      };
       // Two 32-column TMEM loads per wait; a warp whose 32 rows all lie past M reads nothing.
+      // The accumulator is released right after this warp's last TMEM read, before that read's
+      // stores: with a single accumulator the next tile's MMAs are waiting for it.
+      bool released = false;
 #pragma unroll 1
       for (int c = c_begin; c < c_end; c += 2) {
         if (col_tile0 + c * 32 >= p.N || !warp_has_rows) break;   // uniform across the warp
@@ -618,6 +783,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ptx::tmem_ld_32x32b_x32(trow + uint32_t(c * 32), r0);
         if (two) ptx::tmem_ld_32x32b_x32(trow + uint32_t((c + 1) * 32), r1);
         ptx::tmem_wait_ld();
+        const bool last = c + 2 >= c_end || col_tile0 + (c + 2) * 32 >= p.N;
+        if (last) {
+          release_accumulator();
+          released = true;
+        }
         if (p.splits > 1) {
           store_chunk(c, r0);
           if (two) store_chunk(c + 1, r1);
@@ -626,14 +796,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (two) stage_and_store(c + 1, r1);
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (kPair)
-          ptx::mbar_arrive_remote(ptx::mapa_shared(tempty_bar(buf), 0));   // the leader's barrier
-        else
-          ptx::mbar_arrive(tempty_bar(buf));
-      }
+      if (!released) release_accumulator();
       if (++buf == C::ACC_BUFS) {
         buf = 0;
         bphase ^= 1u;

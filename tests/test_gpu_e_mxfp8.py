@@ -98,3 +98,30 @@ def test_mxfp8_llm_shape():
     y_ref, _, sabs = oracle.gemm_mxfp8(x, sx, w, sw, rows=rows)
     check_tolerance(host_bits(y_full)[rows], y_ref, sabs, oracle.TOL_BF16, "MXFP8 LLM shape")
     g.close()
+
+
+@pytest.mark.parametrize("K,N,M,split", [
+    (512, 272, 300, 0),     # last pair tile: 16 columns in the leader's half, none in the peer's
+    (1024, 400, 257, 0),    # last pair tile ends inside the peer's half; M one past a pair tile
+    (2048, 4000, 77, 0),
+    (4096, 512, 300, 4),    # fixed split count on the pair tile
+    (4096, 256, 129, 0),    # one N tile: the automatic split (S = 4 at 152 SMs)
+])
+def test_mxfp8_ragged_and_split(K, N, M, split):
+    """Ragged M and N on the 256 x 256 MXFP8 CTA-pair tile, against the oracle, with the rows
+    of smaller batches bitwise equal to the same rows of the full batch."""
+    x, sx, w, sw = inputs(K, N, ("VAR", "VAR"), rows=M)
+    y_ref, _, sabs = oracle.gemm_mxfp8(x, sx, w, sw)
+    g = BiGemm(K, N, "mxfp8", split_k=split)
+    assert g.config["ctas_per_tile"] == 2 and g.config["block_m"] == 256
+    if split:
+        assert g.config["split_k"] == split
+    xd, sxd, wd, swd = dev_u8(x), dev_u8(sx), dev_u8(w), dev_u8(sw)
+    y = g(xd, wd, sx=sxd, sw=swd)
+    check_tolerance(host_bits(y), y_ref, sabs, oracle.TOL_BF16, f"MXFP8 K={K} N={N} M={M}")
+    for M2 in (1, 2, 128, 129, 256):
+        if M2 < M:
+            y2 = g(xd[:M2], wd, sx=sxd[:M2], sw=swd)
+            assert torch.equal(y2.view(torch.int16), y[:M2].view(torch.int16)), M2
+    assert g.device_error() == 0
+    g.close()

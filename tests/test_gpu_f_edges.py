@@ -117,6 +117,11 @@ def test_argument_errors():
         bg.bi_gemm_run(f.handle, xs.data_ptr(), 4, ws.data_ptr(),
                        bg.bi_gemm_scales(sxs.data_ptr() + 1, sxs.data_ptr()), y.data_ptr(), s)
     assert e.value.code == bg.BI_GEMM_ERR_ALIGNMENT
+    for off in (2, 4, 8):   # W scales are copied in 16-byte chunks
+        with pytest.raises(BiGemmError) as e:
+            bg.bi_gemm_run(f.handle, xs.data_ptr(), 4, ws.data_ptr(),
+                           bg.bi_gemm_scales(sxs.data_ptr(), sxs.data_ptr() + off), y.data_ptr(), s)
+        assert e.value.code == bg.BI_GEMM_ERR_ALIGNMENT
     assert g.device_error() == 0 and f.device_error() == 0
     g.close()
     f.close()
