@@ -29,8 +29,8 @@
 //   warp 0      TMA producer: x tile [128 x BK] (K-major, 128-byte swizzle) and W tile
 //               [BK x BN] (N-major, 128-byte swizzle) per pipeline stage;
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
-//   warps 2-3   (MXFP8 only) scale producers, taking the k-blocks in turn: E8M0 scales into
-//               the tcgen05.cp layout;
+//   warps 2-7   (MXFP8 only) scale producers, taking the k-blocks in turn: E8M0 scales into
+//               the tcgen05.cp layout, then (leader CTA) tcgen05.cp into TMEM;
 //   last 8      epilogue: tcgen05.ld -> round to nearest even -> TMA stores of 32 x 32 blocks,
 //               or fp32 partials + ordered merge when S > 1.
 // Every wait is bounded in time; on expiry the kernel records an error bit in the
@@ -109,11 +109,18 @@ struct KCfg {
   static constexpr int SFB_BYTES = kFp8 ? (BN / 128) * 512 : 0;
   static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
   static constexpr int EPI_WARPS = 8;                   // two per TMEM lane quarter
-  // MXFP8: scale-producer warps take the k-blocks in turn, so that the global-load latency of
-  // several stages' scales overlaps.
-  static constexpr int SCALE_WARPS = kFp8 ? 2 : 0;
+  // MXFP8: six scale-producer warps take the k-blocks in turn, so that the load latency of six
+  // stages' scales overlaps.
+  static constexpr int SCALE_WARPS = kFp8 ? 6 : 0;
   static constexpr int NUM_WARPS = 2 + SCALE_WARPS + EPI_WARPS;
   static constexpr int EPI_WARP0 = NUM_WARPS - EPI_WARPS;
+  // MXFP8 kernels launch 16 warps (128 registers a thread); setmaxnreg then moves registers from
+  // the two producer warpgroups (TMA, MMA, scales) to the two epilogue warpgroups.
+  static constexpr bool kRegSplit = kFp8;
+  static constexpr int REGS_LOW = 80, REGS_HIGH = 176;
+  static_assert(!kRegSplit || (NUM_WARPS == 16 && EPI_WARP0 == 8), "register split: whole warpgroups");
+  static_assert(!kRegSplit || EPI_WARP0 * 32 * REGS_LOW + EPI_WARPS * 32 * REGS_HIGH <= 65536,
+                "register split exceeds the launch's registers");
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int THREADS = NUM_WARPS * 32;
   // TMEM columns: accumulators first, then 16 columns of scale factors per stage.
@@ -125,9 +132,7 @@ struct KCfg {
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-  // MXFP8: per scale warp, two prefetch buffers of one k-block's scales each
-  static constexpr int OFF_SFRAW = OFF_SF + STAGES * SF_BYTES;
-  static constexpr int OFF_BAR = OFF_SFRAW + SCALE_WARPS * 2 * SF_BYTES;
+  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
   // full, empty, accumulator full / empty, drain, epilogue; MXFP8 adds per stage the peer's
   // scales-ready barrier and per scale warp a drain barrier for its scale copies
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 2 + (kFp8 ? STAGES + SCALE_WARPS : 0);
@@ -335,348 +340,342 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   // previous kernel in the stream.  Each role waits for that kernel to complete
   // (grid_dependency_wait) just before its first global-memory access.
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if constexpr (kPair) {
-      if (lane != 0 || rank != 0) ptx::cluster_wait();   // the peer signals the leader's barriers
-    }
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued_mask = 0, issued_par = 0;   // per stage: an issue is outstanding / its parity
-      bool ok = true, dep_done = false;
-      for (int u = group; u < units && ok; u += ngroups) {
-        const UnitCoord uc = unit_coord(u, p);
-        for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
-          if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
-            ok = false;
-            break;
-          }
-          if (!dep_done) {
-            ptx::grid_dependency_wait();
-            dep_done = true;
-          }
-          bool skip = false;
-#ifdef BI_GEMM_CONTROLS
-          // control build only: withhold one stage so that the consumer's bounded wait expires
-          skip = (p.test_flags & 1u) && u == group && kb == uc.kb_begin;
-#endif
-          if (!skip) {
-            const uint32_t fb = full_bar(stage);
-            const uint32_t adst = sbase + C::OFF_A + stage * C::A_BYTES;
-            const uint32_t bdst = sbase + C::OFF_B + stage * C::B_BYTES;
-            const int row0 = uc.m_tile * C::TILE_M + int(rank) * kBM;
-            const int col0 = uc.n_tile * C::BN + int(rank) * C::BN_CTA;
-            // x rows at or past M are never stored, so they need not be loaded: a CTA whose 128
-            // rows all lie past M skips its x tile, and the x box is only as tall as M needs.
-            // The shared-memory rows left unwritten feed only those discarded output rows.
-            const uint32_t a_bytes = uint32_t(p.a_box_rows) * 128u;
-            const bool load_a = row0 < p.M;
-            if constexpr (kPair) {
-              const uint32_t lfb = ptx::mapa_shared(fb, 0);   // the leader's full barrier
-              if (rank == 0) {
-                const bool peer_a = row0 + kBM < p.M;
-                ptx::mbar_arrive_expect_tx(fb, (load_a ? a_bytes : 0u) + (peer_a ? a_bytes : 0u) +
-                                                   uint32_t(C::CTAS * C::B_BYTES));
-              }
-              if (load_a) ptx::tma_load_2d_pair(adst, &tmap_x, lfb, kb * C::BK, row0);
-#pragma unroll
-              for (int a = 0; a < C::N_ATOMS; ++a)
-                ptx::tma_load_2d_pair(bdst + a * C::B_ATOM_BYTES, &tmap_w, lfb, col0 + a * C::ATOM_N,
-                                      kb * C::BK);
-            } else {
-              ptx::mbar_arrive_expect_tx(fb, a_bytes + uint32_t(C::B_BYTES));
-              ptx::tma_load_2d(adst, &tmap_x, fb, kb * C::BK, row0);
-#pragma unroll
-              for (int a = 0; a < C::N_ATOMS; ++a)
-                ptx::tma_load_2d(bdst + a * C::B_ATOM_BYTES, &tmap_w, fb, col0 + a * C::ATOM_N, kb * C::BK);
-            }
-            issued_mask |= 1u << stage;
-            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-          }
-
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      ptx::launch_dependents();   // this CTA has issued all its loads
+  if (warp < C::EPI_WARP0) {
+    // producer warpgroups: TMA, MMA issue (and MXFP8 scales) need few registers
+    if constexpr (C::kRegSplit) ptx::setmaxnreg_dec<C::REGS_LOW>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
       if constexpr (kPair) {
-        if (rank == 0) ptx::cluster_wait();
+        if (lane != 0 || rank != 0) ptx::cluster_wait();   // the peer signals the leader's barriers
       }
-      if (!ok) {
-        // let every copy already in flight land before the CTA can exit
-        if (rank == 0) {
-          SyncCtx drain{abort_flag, p.status, p.timeout_ns};
-          volatile uint32_t no_abort = 0;
-          drain.abort = &no_abort;
-          for (int s = 0; s < C::STAGES; ++s)
-            if (issued_mask & (1u << s))
-              wait_phase(full_bar(s), (issued_par >> s) & 1u, drain, kErrTimeoutProducer);
-        } else if (issued_mask) {
-          // the peer's copies are counted on the leader's barriers: give them time to land
-          const uint64_t t0 = ptx::globaltimer();
-          while (ptx::globaltimer() - t0 < 2000000ull) {
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_par = 0;   // per stage: an issue is outstanding / its parity
+        bool ok = true, dep_done = false;
+        for (int u = group; u < units && ok; u += ngroups) {
+          const UnitCoord uc = unit_coord(u, p);
+          for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
+            if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
+              ok = false;
+              break;
+            }
+            if (!dep_done) {
+              ptx::grid_dependency_wait();
+              dep_done = true;
+            }
+            bool skip = false;
+  #ifdef BI_GEMM_CONTROLS
+            // control build only: withhold one stage so that the consumer's bounded wait expires
+            skip = (p.test_flags & 1u) && u == group && kb == uc.kb_begin;
+  #endif
+            if (!skip) {
+              const uint32_t fb = full_bar(stage);
+              const uint32_t adst = sbase + C::OFF_A + stage * C::A_BYTES;
+              const uint32_t bdst = sbase + C::OFF_B + stage * C::B_BYTES;
+              const int row0 = uc.m_tile * C::TILE_M + int(rank) * kBM;
+              const int col0 = uc.n_tile * C::BN + int(rank) * C::BN_CTA;
+              // x rows at or past M are never stored, so they need not be loaded: a CTA whose 128
+              // rows all lie past M skips its x tile, and the x box is only as tall as M needs.
+              // The shared-memory rows left unwritten feed only those discarded output rows.
+              const uint32_t a_bytes = uint32_t(p.a_box_rows) * 128u;
+              const bool load_a = row0 < p.M;
+              if constexpr (kPair) {
+                const uint32_t lfb = ptx::mapa_shared(fb, 0);   // the leader's full barrier
+                if (rank == 0) {
+                  const bool peer_a = row0 + kBM < p.M;
+                  ptx::mbar_arrive_expect_tx(fb, (load_a ? a_bytes : 0u) + (peer_a ? a_bytes : 0u) +
+                                                     uint32_t(C::CTAS * C::B_BYTES));
+                }
+                if (load_a) ptx::tma_load_2d_pair(adst, &tmap_x, lfb, kb * C::BK, row0);
+  #pragma unroll
+                for (int a = 0; a < C::N_ATOMS; ++a)
+                  ptx::tma_load_2d_pair(bdst + a * C::B_ATOM_BYTES, &tmap_w, lfb, col0 + a * C::ATOM_N,
+                                        kb * C::BK);
+              } else {
+                ptx::mbar_arrive_expect_tx(fb, a_bytes + uint32_t(C::B_BYTES));
+                ptx::tma_load_2d(adst, &tmap_x, fb, kb * C::BK, row0);
+  #pragma unroll
+                for (int a = 0; a < C::N_ATOMS; ++a)
+                  ptx::tma_load_2d(bdst + a * C::B_ATOM_BYTES, &tmap_w, fb, col0 + a * C::ATOM_N, kb * C::BK);
+              }
+              issued_mask |= 1u << stage;
+              issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+            }
+
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        ptx::launch_dependents();   // this CTA has issued all its loads
+        if constexpr (kPair) {
+          if (rank == 0) ptx::cluster_wait();
+        }
+        if (!ok) {
+          // let every copy already in flight land before the CTA can exit
+          if (rank == 0) {
+            SyncCtx drain{abort_flag, p.status, p.timeout_ns};
+            volatile uint32_t no_abort = 0;
+            drain.abort = &no_abort;
+            for (int s = 0; s < C::STAGES; ++s)
+              if (issued_mask & (1u << s))
+                wait_phase(full_bar(s), (issued_par >> s) & 1u, drain, kErrTimeoutProducer);
+          } else if (issued_mask) {
+            // the peer's copies are counted on the leader's barriers: give them time to land
+            const uint64_t t0 = ptx::globaltimer();
+            while (ptx::globaltimer() - t0 < 2000000ull) {
+            }
           }
         }
       }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (leader CTA)
-    if constexpr (kPair) ptx::cluster_wait();            // the peer's TMEM is allocated
-    if (lane == 0 && rank == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int buf = 0;
-      uint32_t bphase = 0;
-      bool ok = true, issued_any = false;
-      for (int u = group; u < units && ok; u += ngroups) {
-        const UnitCoord uc = unit_coord(u, p);
-        if (!wait_phase(tempty_bar(buf), bphase ^ 1u, sc, kErrTimeoutMma)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + uint32_t(buf * C::BN);
-        for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
-          if (!wait_phase(full_bar(stage), phase, sc, kErrTimeoutMma)) {
+      __syncwarp();
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer (leader CTA)
+      if constexpr (kPair) ptx::cluster_wait();            // the peer's TMEM is allocated
+      if (lane == 0 && rank == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int buf = 0;
+        uint32_t bphase = 0;
+        bool ok = true, issued_any = false;
+        for (int u = group; u < units && ok; u += ngroups) {
+          const UnitCoord uc = unit_coord(u, p);
+          if (!wait_phase(tempty_bar(buf), bphase ^ 1u, sc, kErrTimeoutMma)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a_addr = sbase + C::OFF_A + stage * C::A_BYTES;
-          const uint32_t b_addr = sbase + C::OFF_B + stage * C::B_BYTES;
-          if constexpr (C::kFp8) {
-            // the stage's scales are already in TMEM: their copies were committed to full_bar
-            const uint32_t sfa_t = tmem_base + uint32_t(C::SF_TMEM_COL0 + 16 * stage);
-            const uint32_t sfb_t = sfa_t + 8u;
-#pragma unroll
-            for (int kk = 0; kk < C::K_STEPS; ++kk) {
-              const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
-              const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
-                                             8 * C::B_SW, C::B_LAYOUT);
-              const uint32_t idesc = C::IDESC_MXF8 | (uint32_t(kk) << 4) | (uint32_t(kk) << 29);
-              const uint32_t acc = (kb != uc.kb_begin || kk != 0) ? 1u : 0u;
-              if constexpr (kPair)
-                ptx::mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
-              else
-                ptx::mma_mxf8(d_tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
+          const uint32_t d_tmem = tmem_base + uint32_t(buf * C::BN);
+          for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
+            if (!wait_phase(full_bar(stage), phase, sc, kErrTimeoutMma)) {
+              ok = false;
+              break;
             }
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < C::K_STEPS; ++kk) {
-              const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
-              const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
-                                             8 * C::B_SW, C::B_LAYOUT);
-              const uint32_t acc = (kb != uc.kb_begin || kk != 0) ? 1u : 0u;
-              if constexpr (kPair)
-                ptx::mma_bf16_pair(d_tmem, ad, bd, C::IDESC_BF16, acc);
-              else
-                ptx::mma_bf16(d_tmem, ad, bd, C::IDESC_BF16, acc);
-            }
-          }
-          issued_any = true;
-          if constexpr (kPair)
-            ptx::tc_commit_pair_mc(empty_bar(stage), 0x3);   // frees the stage in both CTAs
-          else
-            ptx::tc_commit(empty_bar(stage));
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        if constexpr (kPair)
-          ptx::tc_commit_pair_mc(tfull_bar(buf), 0x3);       // both CTAs' epilogues
-        else
-          ptx::tc_commit(tfull_bar(buf));
-        if (++buf == C::ACC_BUFS) {
-          buf = 0;
-          bphase ^= 1u;
-        }
-      }
-      if (!ok && issued_any) {
-        // wait for the MMAs already issued before TMEM is released
-        if constexpr (kPair)
-          ptx::tc_commit_pair_mc(drain_bar, 0x1);
-        else
-          ptx::tc_commit(drain_bar);
-        SyncCtx drain{abort_flag, p.status, p.timeout_ns};
-        volatile uint32_t no_abort = 0;
-        drain.abort = &no_abort;
-        wait_phase(drain_bar, 0u, drain, kErrTimeoutMma);
-      }
-    }
-    __syncwarp();
-  } else if (C::kFp8 && warp < 2 + C::SCALE_WARPS) {
-    if constexpr (C::kFp8) {
-      // ---------------------------------------------------------- scale producers (MXFP8)
-      if constexpr (kPair) ptx::cluster_wait();
-      // Layout expected by tcgen05.cp 32x128b.warpx4 for 128 rows x 4 k-blocks (512 bytes):
-      // byte (r % 32) * 16 + (r / 32) * 4 + kblk.  One 512-byte block for this CTA's 128 rows
-      // of x, one per 128 columns of the tile's W columns (all BN of them, on a pair too).
-      // This CTA's k-block items are numbered it = 0, 1, ... in pipeline order; scale warp j
-      // fills items j, j + SCALE_WARPS, ...  While it waits for an item's stage, a warp already
-      // has its next item's scales on the way into shared memory (cp.async).
-      // On a pair the peer's warp publishes its stage to the leader (sfpeer_bar); the leader's
-      // warp then issues the tcgen05.cp of both CTAs' scales and commits them to the stage's
-      // full barrier, so the MMA issuer finds the scales in TMEM and issues only MMAs.
-      const int sw_id = warp - 2;
-      const int KB32 = p.K / 32;
-      int u = group, kb = 0, kb_end = 0, row_base = 0, col_base = 0;
-      auto enter_unit = [&]() {
-        const UnitCoord uc = unit_coord(u, p);
-        kb = uc.kb_begin;
-        kb_end = uc.kb_end;
-        row_base = uc.m_tile * C::TILE_M + int(rank) * kBM;
-        col_base = uc.n_tile * C::BN;
-      };
-      // step to the next item; false once this CTA has none left
-      auto advance = [&]() -> bool {
-        ++kb;
-        while (kb >= kb_end) {
-          u += ngroups;
-          if (u >= units) return false;
-          enter_unit();
-        }
-        return true;
-      };
-      // Prefetch buffer: [x scales, 512 B, already in the tcgen05.cp layout | W scales as stored:
-      // 4 rows x BN bytes].  Filled by cp.async, so the warp never waits on the loads in flight.
-      const uint32_t raw0 = sbase + C::OFF_SFRAW + uint32_t(sw_id * 2 * C::SF_BYTES);
-      constexpr int kChunksPerRow = C::BN / 16;                   // 16-byte chunks per W scale row
-      auto load = [&](uint32_t raw) {
-        // x: this k-block's four scales of a row (one 32-bit word) go straight to the row's place
-        // in the layout; rows at or past M are zero-filled (their outputs are never stored)
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int r = g * 32 + lane;
-          const int row = row_base + r;
-          const bool in = row < p.M;
-          ptx::cp_async_4(raw + uint32_t((r & 31) * 16 + (r >> 5) * 4),
-                          in ? p.sx + (size_t)row * KB32 + 4 * kb : p.sx, in ? 4u : 0u);
-        }
-        // W: the four scale rows of this k-block over the tile's BN columns, in 16-byte chunks;
-        // columns at or past N (whole chunks, N % 16 == 0) are zero-filled (never stored)
-#pragma unroll
-        for (int i = 0; i < C::BN / 128; ++i) {
-          const int c = i * 32 + lane;
-          const int t = c / kChunksPerRow, cc = c - t * kChunksPerRow;
-          const int col = col_base + cc * 16;
-          const bool in = col < p.N;
-          ptx::cp_async_16(raw + uint32_t(C::SFA_BYTES + t * C::BN + cc * 16),
-                           in ? p.sw + (size_t)(kb * 4 + t) * p.N + col : p.sw, in ? 16u : 0u);
-        }
-        ptx::cp_async_commit();
-      };
-      ptx::grid_dependency_wait();
-      bool ok = true, copied = false;   // lane 0: no wait gave up / issued scale copies
-      bool valid = u < units;
-      if (valid) enter_unit();
-      for (int i = 0; i < sw_id && valid; ++i) valid = advance();
-      int it = sw_id;
-      uint32_t buf = 0;
-      if (valid) load(raw0);
-      while (valid) {
-        const int stage = it % C::STAGES;
-        const uint32_t phase = uint32_t(it / C::STAGES) & 1u;
-        const uint32_t raw = raw0 + buf * C::SF_BYTES;
-        // prefetch this warp's next k-block into the other buffer (its data was consumed last time)
-        bool next = true;
-        for (int i = 0; i < C::SCALE_WARPS && next; ++i) next = advance();
-        if (next) load(raw0 + (buf ^ 1u) * C::SF_BYTES);
-        if (!warp_wait_phase<Wait::kRelaxed>(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutScales)) break;
-        if (next)
-          ptx::cp_async_wait<1>();       // this k-block's copies have landed
-        else
-          ptx::cp_async_wait<0>();
-        __syncwarp();                    // ... for every lane's copies
-        const uint32_t sf_addr = sbase + C::OFF_SF + stage * C::SF_BYTES;
-        {
-          uint32_t a0, a1, a2, a3;
-          ptx::ld_shared_v4(raw + lane * 16, a0, a1, a2, a3);
-          ptx::st_shared_v4(sf_addr + lane * 16, a0, a1, a2, a3);
-        }
-#pragma unroll
-        for (int b = 0; b < C::BN / 128; ++b) {
-          // lane l takes columns 4l .. 4l+3 of each scale row; a 4 x 4 byte transpose gives v[j],
-          // the four k-block scales of column 4l + j
-          uint32_t w[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) w[t] = ptx::ld_shared_u32(raw + C::SFA_BYTES + t * C::BN + b * 128 + 4 * lane);
-          const uint32_t lo01 = __byte_perm(w[0], w[1], 0x5140);
-          const uint32_t hi01 = __byte_perm(w[0], w[1], 0x7362);
-          const uint32_t lo23 = __byte_perm(w[2], w[3], 0x5140);
-          const uint32_t hi23 = __byte_perm(w[2], w[3], 0x7362);
-          const uint32_t v[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
-                                 __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
-          const uint32_t blk = sf_addr + C::SFA_BYTES + b * 512;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c = 4 * lane + j;                    // column within this 128-column block
-            ptx::st_shared_u32(blk + (c & 31) * 16 + (c >> 5) * 4, v[j]);
-          }
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (kPair && rank != 0) {
-            // peer: publish this stage's scales to the leader, which copies them into TMEM
-            ptx::fence_release_shared();
-            ptx::mbar_arrive_remote_relaxed(ptx::mapa_shared(sfpeer_bar(stage), 0));
-          } else {
-            // leader (or single CTA): once the peer's scales are in place too, copy both CTAs'
-            // scales into TMEM and count the copies' completion on the stage's full barrier
-            bool ready = true;
-            if constexpr (kPair) ready = wait_phase<Wait::kCluster>(sfpeer_bar(stage), phase, sc, kErrTimeoutScales);
-            if (ready) {
-              ptx::tc_fence_after();
+            ptx::tc_fence_after();
+            const uint32_t a_addr = sbase + C::OFF_A + stage * C::A_BYTES;
+            const uint32_t b_addr = sbase + C::OFF_B + stage * C::B_BYTES;
+            if constexpr (C::kFp8) {
+              // the stage's scales are already in TMEM: their copies were committed to full_bar
               const uint32_t sfa_t = tmem_base + uint32_t(C::SF_TMEM_COL0 + 16 * stage);
               const uint32_t sfb_t = sfa_t + 8u;
-              const uint64_t sfa_d = make_sdesc(sf_addr, 0, 128, kLayoutNone);
-              if constexpr (kPair)
-                ptx::tc_cp_32x128b_x4_pair(sfa_t, sfa_d);
-              else
-                ptx::tc_cp_32x128b_x4(sfa_t, sfa_d);
-#pragma unroll
-              for (int b = 0; b < C::BN / 128; ++b) {
-                const uint64_t sfb_d = make_sdesc(sf_addr + C::SFA_BYTES + 512 * b, 0, 128, kLayoutNone);
+  #pragma unroll
+              for (int kk = 0; kk < C::K_STEPS; ++kk) {
+                const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
+                const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
+                                               8 * C::B_SW, C::B_LAYOUT);
+                const uint32_t idesc = C::IDESC_MXF8 | (uint32_t(kk) << 4) | (uint32_t(kk) << 29);
+                const uint32_t acc = (kb != uc.kb_begin || kk != 0) ? 1u : 0u;
                 if constexpr (kPair)
-                  ptx::tc_cp_32x128b_x4_pair(sfb_t + 4u * b, sfb_d);
+                  ptx::mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
                 else
-                  ptx::tc_cp_32x128b_x4(sfb_t + 4u * b, sfb_d);
+                  ptx::mma_mxf8(d_tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
               }
-              if constexpr (kPair)
-                ptx::tc_commit_pair_mc(full_bar(stage), 0x1);
-              else
-                ptx::tc_commit(full_bar(stage));
-              copied = true;
+            } else {
+  #pragma unroll
+              for (int kk = 0; kk < C::K_STEPS; ++kk) {
+                const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
+                const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
+                                               8 * C::B_SW, C::B_LAYOUT);
+                const uint32_t acc = (kb != uc.kb_begin || kk != 0) ? 1u : 0u;
+                if constexpr (kPair)
+                  ptx::mma_bf16_pair(d_tmem, ad, bd, C::IDESC_BF16, acc);
+                else
+                  ptx::mma_bf16(d_tmem, ad, bd, C::IDESC_BF16, acc);
+              }
             }
-            ok = ready;
+            issued_any = true;
+            if constexpr (kPair)
+              ptx::tc_commit_pair_mc(empty_bar(stage), 0x3);   // frees the stage in both CTAs
+            else
+              ptx::tc_commit(empty_bar(stage));
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if constexpr (kPair)
+            ptx::tc_commit_pair_mc(tfull_bar(buf), 0x3);       // both CTAs' epilogues
+          else
+            ptx::tc_commit(tfull_bar(buf));
+          if (++buf == C::ACC_BUFS) {
+            buf = 0;
+            bphase ^= 1u;
           }
         }
-        if (!__shfl_sync(0xffffffffu, ok ? 1u : 0u, 0)) break;
-        it += C::SCALE_WARPS;
-        buf ^= 1u;
-        valid = next;
+        if (!ok && issued_any) {
+          // wait for the MMAs already issued before TMEM is released
+          if constexpr (kPair)
+            ptx::tc_commit_pair_mc(drain_bar, 0x1);
+          else
+            ptx::tc_commit(drain_bar);
+          SyncCtx drain{abort_flag, p.status, p.timeout_ns};
+          volatile uint32_t no_abort = 0;
+          drain.abort = &no_abort;
+          wait_phase(drain_bar, 0u, drain, kErrTimeoutMma);
+        }
       }
-      ptx::cp_async_wait<0>();   // no copy may still target shared memory when the CTA exits
-      // the last scale copies must land before the CTA may release TMEM
-      if (lane == 0 && copied) {
-        if constexpr (kPair)
-          ptx::tc_commit_pair_mc(sfdrain_bar(sw_id), 0x1);
-        else
-          ptx::tc_commit(sfdrain_bar(sw_id));
-        SyncCtx drain{abort_flag, p.status, p.timeout_ns};
-        volatile uint32_t no_abort = 0;
-        drain.abort = &no_abort;
-        wait_phase(sfdrain_bar(sw_id), 0u, drain, kErrTimeoutScales);
+      __syncwarp();
+    } else if (C::kFp8 && warp < 2 + C::SCALE_WARPS) {
+      if constexpr (C::kFp8) {
+        // ---------------------------------------------------------- scale producers (MXFP8)
+        if constexpr (kPair) ptx::cluster_wait();
+        // Layout expected by tcgen05.cp 32x128b.warpx4 for 128 rows x 4 k-blocks (512 bytes):
+        // byte (r % 32) * 16 + (r / 32) * 4 + kblk.  One 512-byte block for this CTA's 128 rows
+        // of x, one per 128 columns of the tile's W columns (all BN of them, on a pair too).
+        // This CTA's k-block items are numbered it = 0, 1, ... in pipeline order; scale warp j
+        // fills items j, j + SCALE_WARPS, ...: once the item's stage is free it copies the scales
+        // into the stage (cp.async) and rearranges them there.
+        // On a pair the peer's warp publishes its stage to the leader (sfpeer_bar); the leader's
+        // warp then issues the tcgen05.cp of both CTAs' scales and commits them to the stage's
+        // full barrier, so the MMA issuer finds the scales in TMEM and issues only MMAs.
+        const int sw_id = warp - 2;
+        const int KB32 = p.K / 32;
+        int u = group, kb = 0, kb_end = 0, row_base = 0, col_base = 0;
+        auto enter_unit = [&]() {
+          const UnitCoord uc = unit_coord(u, p);
+          kb = uc.kb_begin;
+          kb_end = uc.kb_end;
+          row_base = uc.m_tile * C::TILE_M + int(rank) * kBM;
+          col_base = uc.n_tile * C::BN;
+        };
+        // step to the next item; false once this CTA has none left
+        auto advance = [&]() -> bool {
+          ++kb;
+          while (kb >= kb_end) {
+            u += ngroups;
+            if (u >= units) return false;
+            enter_unit();
+          }
+          return true;
+        };
+        constexpr int kChunksPerRow = C::BN / 16;                   // 16-byte chunks per W scale row
+        ptx::grid_dependency_wait();
+        bool ok = true, copied = false;   // lane 0: no wait gave up / issued scale copies
+        bool valid = u < units;
+        if (valid) enter_unit();
+        for (int i = 0; i < sw_id && valid; ++i) valid = advance();
+        int it = sw_id;
+        while (valid) {
+          const int stage = it % C::STAGES;
+          const uint32_t phase = uint32_t(it / C::STAGES) & 1u;
+          if (!warp_wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutScales)) break;
+          const uint32_t sf_addr = sbase + C::OFF_SF + stage * C::SF_BYTES;
+          const uint32_t sfb_addr = sf_addr + C::SFA_BYTES;
+          // x: this k-block's four scales of a row (one 32-bit word) go straight to the row's place
+          // in the layout; rows at or past M are zero-filled (their outputs are never stored)
+  #pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int r = g * 32 + lane;
+            const int row = row_base + r;
+            const bool in = row < p.M;
+            ptx::cp_async_4(sf_addr + uint32_t((r & 31) * 16 + (r >> 5) * 4),
+                            in ? p.sx + (size_t)row * KB32 + 4 * kb : p.sx, in ? 4u : 0u);
+          }
+          // W: the four scale rows of this k-block over the tile's BN columns, as stored (4 rows x
+          // BN bytes), in 16-byte chunks; columns at or past N (whole chunks, N % 16 == 0) are
+          // zero-filled (never stored)
+  #pragma unroll
+          for (int i = 0; i < C::BN / 128; ++i) {
+            const int c = i * 32 + lane;
+            const int t = c / kChunksPerRow, cc = c - t * kChunksPerRow;
+            const int col = col_base + cc * 16;
+            const bool in = col < p.N;
+            ptx::cp_async_16(sfb_addr + uint32_t(t * C::BN + cc * 16),
+                             in ? p.sw + (size_t)(kb * 4 + t) * p.N + col : p.sw, in ? 16u : 0u);
+          }
+          ptx::cp_async_commit();
+          ptx::cp_async_wait<0>();
+          __syncwarp();                    // every lane's copies have landed
+          // W scales, in place: lane l reads columns 4l .. 4l+3 of each scale row of each
+          // 128-column block; a 4 x 4 byte transpose gives v[b][j], the four k-block scales of
+          // column 4l + j; all reads precede all writes
+          uint32_t v[C::BN / 128][4];
+  #pragma unroll
+          for (int b = 0; b < C::BN / 128; ++b) {
+            uint32_t w[4];
+  #pragma unroll
+            for (int t = 0; t < 4; ++t) w[t] = ptx::ld_shared_u32(sfb_addr + t * C::BN + b * 128 + 4 * lane);
+            const uint32_t lo01 = __byte_perm(w[0], w[1], 0x5140);
+            const uint32_t hi01 = __byte_perm(w[0], w[1], 0x7362);
+            const uint32_t lo23 = __byte_perm(w[2], w[3], 0x5140);
+            const uint32_t hi23 = __byte_perm(w[2], w[3], 0x7362);
+            v[b][0] = __byte_perm(lo01, lo23, 0x5410);
+            v[b][1] = __byte_perm(lo01, lo23, 0x7632);
+            v[b][2] = __byte_perm(hi01, hi23, 0x5410);
+            v[b][3] = __byte_perm(hi01, hi23, 0x7632);
+          }
+          __syncwarp();
+  #pragma unroll
+          for (int b = 0; b < C::BN / 128; ++b) {
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c = 4 * lane + j;                    // column within this 128-column block
+              ptx::st_shared_u32(sfb_addr + b * 512 + (c & 31) * 16 + (c >> 5) * 4, v[b][j]);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (kPair && rank != 0) {
+              // peer: publish this stage's scales to the leader, which copies them into TMEM
+              ptx::fence_release_shared();
+              ptx::mbar_arrive_remote_relaxed(ptx::mapa_shared(sfpeer_bar(stage), 0));
+            } else {
+              // leader (or single CTA): once the peer's scales are in place too, copy both CTAs'
+              // scales into TMEM and count the copies' completion on the stage's full barrier
+              bool ready = true;
+              if constexpr (kPair) ready = wait_phase<Wait::kCluster>(sfpeer_bar(stage), phase, sc, kErrTimeoutScales);
+              if (ready) {
+                ptx::tc_fence_after();
+                const uint32_t sfa_t = tmem_base + uint32_t(C::SF_TMEM_COL0 + 16 * stage);
+                const uint32_t sfb_t = sfa_t + 8u;
+                const uint64_t sfa_d = make_sdesc(sf_addr, 0, 128, kLayoutNone);
+                if constexpr (kPair)
+                  ptx::tc_cp_32x128b_x4_pair(sfa_t, sfa_d);
+                else
+                  ptx::tc_cp_32x128b_x4(sfa_t, sfa_d);
+  #pragma unroll
+                for (int b = 0; b < C::BN / 128; ++b) {
+                  const uint64_t sfb_d = make_sdesc(sf_addr + C::SFA_BYTES + 512 * b, 0, 128, kLayoutNone);
+                  if constexpr (kPair)
+                    ptx::tc_cp_32x128b_x4_pair(sfb_t + 4u * b, sfb_d);
+                  else
+                    ptx::tc_cp_32x128b_x4(sfb_t + 4u * b, sfb_d);
+                }
+                if constexpr (kPair)
+                  ptx::tc_commit_pair_mc(full_bar(stage), 0x1);
+                else
+                  ptx::tc_commit(full_bar(stage));
+                copied = true;
+              }
+              ok = ready;
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, ok ? 1u : 0u, 0)) break;
+          for (int i = 0; i < C::SCALE_WARPS && valid; ++i) valid = advance();
+          it += C::SCALE_WARPS;
+        }
+        ptx::cp_async_wait<0>();   // no copy may still target shared memory when the CTA exits
+        // the last scale copies must land before the CTA may release TMEM
+        if (lane == 0 && copied) {
+          if constexpr (kPair)
+            ptx::tc_commit_pair_mc(sfdrain_bar(sw_id), 0x1);
+          else
+            ptx::tc_commit(sfdrain_bar(sw_id));
+          SyncCtx drain{abort_flag, p.status, p.timeout_ns};
+          volatile uint32_t no_abort = 0;
+          drain.abort = &no_abort;
+          wait_phase(sfdrain_bar(sw_id), 0u, drain, kErrTimeoutScales);
+        }
       }
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp >= C::EPI_WARP0) {
+  } else {
+    // epilogue warpgroups: take the registers the producers gave back
+    if constexpr (C::kRegSplit) ptx::setmaxnreg_inc<C::REGS_HIGH>();
     // ------------------------------------------------------------ epilogue
     if constexpr (kPair) ptx::cluster_wait();
     const int q = warp & 3;                 // TMEM lane quarter this warp may access

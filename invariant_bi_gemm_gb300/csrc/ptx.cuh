@@ -328,6 +328,17 @@ __device__ __forceinline__ void launch_dependents() {
 
 // ------------------------------------------------------------------ misc
 
+// Warp-specialised register split: a warpgroup gives registers back to the SM's pool (dec) or
+// takes them (inc).  The sum over all warps must stay within what the block was launched with.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
