@@ -117,7 +117,9 @@ struct KCfg {
   // MXFP8 kernels launch 16 warps (128 registers a thread); setmaxnreg then moves registers from
   // the two producer warpgroups (TMA, MMA, scales) to the two epilogue warpgroups.
   static constexpr bool kRegSplit = kFp8;
-  static constexpr int REGS_LOW = 80, REGS_HIGH = 176;
+  // (the single-accumulator epilogue holds a warp's whole share of the tile in registers)
+  static constexpr int REGS_LOW = ACC_BUFS == 1 ? 64 : 80;
+  static constexpr int REGS_HIGH = ACC_BUFS == 1 ? 192 : 176;
   static_assert(!kRegSplit || (NUM_WARPS == 16 && EPI_WARP0 == 8), "register split: whole warpgroups");
   static_assert(!kRegSplit || EPI_WARP0 * 32 * REGS_LOW + EPI_WARPS * 32 * REGS_HIGH <= 65536,
                 "register split exceeds the launch's registers");
@@ -757,6 +759,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         stg_next = (stg_next + 1) % C::STG_BUFS;
       };
+      // The same for a block already rounded to bf16 pairs (16 words per row).
+      auto stage_and_store_packed = [&](int c, const uint32_t (&pk)[16]) {
+        const uint32_t dst = stg_base + uint32_t(stg_next * C::STG_BYTES);
+        if (lane == 0) ptx::bulk_wait_read<C::STG_BUFS - 1>();
+        __syncwarp();
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          ptx::st_shared_v4(dst + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4), pk[4 * v], pk[4 * v + 1],
+                            pk[4 * v + 2], pk[4 * v + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&tmap_y, dst, col_tile0 + c * 32, row - lane);
+          ptx::bulk_commit();
+        }
+        stg_next = (stg_next + 1) % C::STG_BUFS;
+      };
       // Tell the MMA issuer this warp has read its part of the accumulator.
       auto release_accumulator = [&]() {
         ptx::tc_fence_before();
@@ -770,6 +789,36 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
         }
       };
+      constexpr int kHalfChunks = kChunks / 2;      // 32-column chunks per warp
+      constexpr bool kPackedRelease = C::ACC_BUFS == 1 && C::kRegSplit && !C::kOutF32;
+      if (kPackedRelease && p.splits == 1) {
+        // Single accumulator (the next tile's MMAs wait for it): read all of this warp's chunks
+        // out of TMEM, rounded to bf16 pairs in registers, release the accumulator, and only
+        // then stage and store them while the next tile's MMAs run.
+        uint32_t pk[kHalfChunks][16];
+        const int nvalid =
+            warp_has_rows ? max(0, min(kHalfChunks, (p.N - col_tile0 + 31) / 32 - c_begin)) : 0;
+#pragma unroll
+        for (int j = 0; j < kHalfChunks; ++j) {
+          if (j < nvalid) {                          // uniform across the warp
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(trow + uint32_t((c_begin + j) * 32), r);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int v = 0; v < 16; ++v)
+              pk[j][v] = ptx::pack_bf16x2_ordered(__uint_as_float(r[2 * v]), __uint_as_float(r[2 * v + 1]));
+          }
+        }
+        release_accumulator();
+#pragma unroll
+        for (int j = 0; j < kHalfChunks; ++j)
+          if (j < nvalid) stage_and_store_packed(c_begin + j, pk[j]);
+        if (++buf == C::ACC_BUFS) {
+          buf = 0;
+          bphase ^= 1u;
+        }
+        continue;                                  // no split-K merge on this path
+      } else {
       // Two 32-column TMEM loads per wait; a warp whose 32 rows all lie past M reads nothing.
       // The accumulator is released right after this warp's last TMEM read, before that read's
       // stores: with a single accumulator the next tile's MMAs are waiting for it.
@@ -790,12 +839,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (p.splits > 1) {
           store_chunk(c, r0);
           if (two) store_chunk(c + 1, r1);
-        } else {
+        } else if constexpr (!kPackedRelease) {      // (unsplit tiles take the path above)
           stage_and_store(c, r0);
           if (two) stage_and_store(c + 1, r1);
         }
       }
       if (!released) release_accumulator();
+      }
       if (++buf == C::ACC_BUFS) {
         buf = 0;
         bphase ^= 1u;
@@ -821,7 +871,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (last) {
           // The (row, 4-column group) items of this 128-row sub-tile are spread over all epilogue
           // threads; each item sums its S partials strictly in split order,
-          // ((p0 + p1) + p2) + ..., with the loads issued in independent batches of 16.
+          // ((p0 + p1) + p2) + ..., with the loads issued in independent batches (16, or 8
+          // where the epilogue shares its register budget).
           __threadfence();
           const int row0 = uc.m_tile * C::TILE_M + int(rank) * kBM;
           const int rows = min(kBM, p.M - row0);
@@ -833,14 +884,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int rr = it / groups, g4 = it - rr * groups;
             const float* sp = src0 + (size_t)rr * C::BN + g4 * 4;
             float4 acc = __ldcg(reinterpret_cast<const float4*>(sp));
+            constexpr int kMergeBatch = C::kRegSplit ? 8 : 16;   // loads in flight per item
 #pragma unroll 1
-            for (int s0 = 1; s0 < p.splits; s0 += 16) {
-              float4 t[16];
+            for (int s0 = 1; s0 < p.splits; s0 += kMergeBatch) {
+              float4 t[kMergeBatch];
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
+              for (int j = 0; j < kMergeBatch; ++j)
                 if (s0 + j < p.splits) t[j] = __ldcg(reinterpret_cast<const float4*>(sp + (s0 + j) * sstride));
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
+              for (int j = 0; j < kMergeBatch; ++j) {
                 if (s0 + j < p.splits) {
                   acc.x = acc.x + t[j].x;
                   acc.y = acc.y + t[j].y;

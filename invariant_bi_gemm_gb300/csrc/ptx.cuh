@@ -402,5 +402,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// pack_bf16x2 kept in program order with the surrounding volatile asm (TMEM loads): a caller can
+// round one chunk before it loads the next, so that raw chunks do not pile up in registers.
+__device__ __forceinline__ uint32_t pack_bf16x2_ordered(float lo, float hi) {
+  uint32_t r;
+  asm volatile("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 }  // namespace ptx
 }  // namespace bigemm
