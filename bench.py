@@ -496,6 +496,41 @@ def measure_other_paths(dev, peaks):
     return out
 
 
+def run_mxfp8_only(args):
+    """Launch only the MXFP8 LLM-shape GEMM (E4M3 x[M,4096]·W[4096,14336], K-varying E8M0
+    scales, bf16 out) at one M, eagerly: --warmup + --steps launches.  For profiling; prints the
+    average launch time as one JSON line (not the benchmark line)."""
+    import torch
+
+    import inputgen as ig
+    from invariant_bi_gemm_gb300 import BiGemm
+
+    dev = torch.device("cuda", 0)
+    M = args.mxfp8_only_m
+    x8 = torch.from_numpy(ig.normal_e4m3(ig.SEED_X, M, K_DIM)).to(dev)
+    sx = torch.from_numpy(ig.e8m0_scales("VAR", ig.SEED_X, M, K_DIM // 32)).to(dev)
+    w8 = torch.from_numpy(ig.normal_e4m3(ig.SEED_W, K_DIM, N_DIM)).to(dev)
+    sw = torch.from_numpy(ig.e8m0_scales("VAR", ig.SEED_W, K_DIM // 32, N_DIM)).to(dev)
+    y = torch.empty((M, N_DIM), dtype=torch.bfloat16, device=dev)
+    g = BiGemm(K_DIM, N_DIM, "mxfp8")
+    for _ in range(args.warmup):
+        g(x8, w8, y, sx=sx, sw=sw)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        g(x8, w8, y, sx=sx, sw=sw)
+    b.record()
+    torch.cuda.synchronize()
+    t = a.elapsed_time(b) / 1e3 / max(1, args.steps)
+    err = g.device_error()
+    print(json.dumps({"mxfp8_only_m": M, "us_per_launch": round(t * 1e6, 2),
+                      "tflops": round(flops(M) / t / 1e12, 1), "device_error": err}))
+    g.close()
+    if err != 0:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -507,7 +542,12 @@ def main():
     ap.add_argument("--no-paths", action="store_true")
     ap.add_argument("--only-m", type=int, default=0,
                     help="time a single M of the sweep only (for profiling); skips e2e, paths, CPU")
+    ap.add_argument("--mxfp8-only-m", type=int, default=0,
+                    help="launch only the MXFP8 LLM-shape GEMM at this M (for profiling)")
     args = ap.parse_args()
+    if args.mxfp8_only_m:
+        run_mxfp8_only(args)
+        return
     if args.only_m:
         global M_SWEEP
         M_SWEEP = [args.only_m]
