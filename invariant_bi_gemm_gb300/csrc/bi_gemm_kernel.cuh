@@ -52,6 +52,7 @@ enum : uint32_t {
   kErrTimeoutMma = 2u,
   kErrTimeoutEpilogue = 4u,
   kErrTimeoutScales = 8u,
+  kErrTimeoutMerge = 16u,
 };
 
 struct KParams {
@@ -67,6 +68,8 @@ struct KParams {
   int32_t kblocks;          // KB = ceil(K / BK)
   int32_t a_box_rows;       // rows per x TMA box: 128, or round_up(M, 8) when M < 128
   int32_t group_n;          // raster order: N tiles per group (M tiles vary fastest within it)
+  int32_t coop_merge;       // S > 1 and every unit has its own resident CTA group: the S split
+                            // CTAs of a sub-tile share its merge (else the last to arrive merges)
   uint64_t timeout_ns;
   uint32_t test_flags;      // only read by the control build
 };
@@ -124,6 +127,7 @@ struct KCfg {
   static_assert(!kRegSplit || EPI_WARP0 * 32 * REGS_LOW + EPI_WARPS * 32 * REGS_HIGH <= 65536,
                 "register split exceeds the launch's registers");
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+  static_assert(EPI_THREADS == 256, "the host's merge-sharing rule assumes 256 epilogue threads");
   static constexpr int THREADS = NUM_WARPS * 32;
   // TMEM columns: accumulators first, then 16 columns of scale factors per stage.
   static constexpr int SF_TMEM_COL0 = ACC_BUFS * BN;
@@ -851,7 +855,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         bphase ^= 1u;
       }
       if (p.splits > 1) {
-        // Fixed-order merge of the S partials by the last CTA to arrive at this sub-tile.
+        // Fixed-order merge of the S partials of this sub-tile: every output element sums its S
+        // partials strictly in split order, ((p0 + p1) + p2) + ..., whoever computes it.  When
+        // every unit has its own resident CTA group (coop_merge), the S split CTAs wait for one
+        // another and each merges 1/S of the elements; otherwise the last CTA to arrive (an
+        // integer counter) merges them all.
         // Hand-off 1: every partial of this CTA is stored and fenced before the count.
         __threadfence();
         __syncwarp();
@@ -859,28 +867,52 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!warp_wait_phase(epi_bar, ephase, sc, kErrTimeoutEpilogue)) break;
         ephase ^= 1u;
         if (epi_tid == 0) {
-          const uint32_t old = atomicAdd(p.counters + sub, 1u);
-          *last_flag = (old == uint32_t(p.splits - 1)) ? 1u : 0u;
+          uint32_t* cnt = p.counters + sub;
+          const uint32_t S = uint32_t(p.splits);
+          const uint32_t old = atomicAdd(cnt, 1u);
+          uint32_t verdict = (old == S - 1) ? 1u : 0u;
+          if (p.coop_merge) {
+            // arrivals count 0 .. S; then departures S .. 2S, and the last one out resets the
+            // counter for the next launch (every CTA has seen S by then)
+            const uint64_t t0 = ptx::globaltimer();
+            verdict = 1u;
+            for (uint32_t spin = 0; ptx::ld_acquire_gpu(cnt) < S; ++spin) {
+              if ((spin & 63u) == 63u && (*abort_flag || ptx::globaltimer() - t0 > p.timeout_ns)) {
+                *abort_flag = 1u;
+                atomicOr(p.status, kErrTimeoutMerge);
+                verdict = 0u;
+                break;
+              }
+            }
+            if (verdict && atomicAdd(cnt, 1u) == 2 * S - 1) atomicExch(cnt, 0u);
+          }
+          *last_flag = verdict;
         }
         // Hand-off 2: the verdict is visible to all four warps.
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(epi_bar);
         if (!warp_wait_phase(epi_bar, ephase, sc, kErrTimeoutEpilogue)) break;
         ephase ^= 1u;
-        const bool last = *last_flag != 0u;
-        if (last) {
-          // The (row, 4-column group) items of this 128-row sub-tile are spread over all epilogue
-          // threads; each item sums its S partials strictly in split order,
-          // ((p0 + p1) + p2) + ..., with the loads issued in independent batches (16, or 8
-          // where the epilogue shares its register budget).
+        const bool merge = *last_flag != 0u;
+        if (merge) {
+          // (row, 4-column group) items, spread over the merging CTA(s)' epilogue threads, with
+          // the loads issued in independent batches (16, or 8 where the epilogue shares its
+          // register budget)
           __threadfence();
           const int row0 = uc.m_tile * C::TILE_M + int(rank) * kBM;
           const int rows = min(kBM, p.M - row0);
           const int groups = (min(C::BN, p.N - col_tile0) + 3) / 4;
+          const int items = rows * groups;
+          int it_begin = 0, it_end = items;
+          if (p.coop_merge) {
+            const int per = (items + p.splits - 1) / p.splits;
+            it_begin = min(items, uc.s * per);
+            it_end = min(items, it_begin + per);
+          }
           const float* src0 = p.ws + ((size_t)sub * p.splits) * kBM * C::BN;
           const size_t sstride = (size_t)kBM * C::BN;
 #pragma unroll 1
-          for (int it = epi_tid; it < rows * groups; it += C::EPI_THREADS) {
+          for (int it = it_begin + epi_tid; it < it_end; it += C::EPI_THREADS) {
             const int rr = it / groups, g4 = it - rr * groups;
             const float* sp = src0 + (size_t)rr * C::BN + g4 * 4;
             float4 acc = __ldcg(reinterpret_cast<const float4*>(sp));
@@ -911,7 +943,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.y) + yo) = pk;
             }
           }
-          if (epi_tid == 0) p.counters[sub] = 0u;   // ready for the next launch
+          if (!p.coop_merge && epi_tid == 0) p.counters[sub] = 0u;   // ready for the next launch
         }
         // Hand-off 3: last_flag may be rewritten only after every warp has read it.
         __syncwarp();

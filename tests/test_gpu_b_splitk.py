@@ -64,3 +64,21 @@ def test_forced_split_counts_agree_with_oracle(setup):
         y = host_bits(g(Xd[:130].contiguous(), Wd))
         check_tolerance(y, y_ref[:130], sabs[:130], oracle.TOL_F32, f"S={s}")
         g.close()
+
+
+@pytest.mark.parametrize("max_ctas", [4, 16, 31])
+def test_merge_paths_give_identical_bits(setup, max_ctas):
+    """With every split unit resident the 32 split CTAs share a tile's merge; with the grid
+    capped below the unit count the last CTA to arrive merges it alone.  Both sum every element
+    in split order, so the outputs are bitwise identical (and the capped grid also exercises
+    CTAs that carry several units)."""
+    g, Wd, Xd, _, _ = setup
+    capped = BiGemm(K, N, "bf16_f32", max_ctas=max_ctas)
+    assert capped.config["split_k"] == 32 and capped.config["max_groups"] == max_ctas
+    for M in (1, 64, 129, 256):
+        xs = Xd[:M].contiguous()
+        a = host_bits(g(xs, Wd))
+        b = host_bits(capped(xs, Wd))
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (M, max_ctas)
+    assert capped.device_error() == 0 and g.device_error() == 0
+    capped.close()
