@@ -110,3 +110,14 @@ BI_CTL_API int bi_ctl_run_stall(bi_gemm_t h, const void* x, int64_t M, const voi
   std::lock_guard<std::mutex> lk(h->mu);
   return launch(h, x, M, W, scales, y, static_cast<cudaStream_t>(stream), 0, 1u);
 }
+
+// Failure injection for the shared split-K merge: split 0 of every tile never counts its
+// arrival, so the other split CTAs' bounded waits for it expire; the kernel must record
+// BI_GEMM_ERR_TIMEOUT and return, and the next run must reset the arrival counters.
+BI_CTL_API int bi_ctl_run_skip_arrival(bi_gemm_t h, const void* x, int64_t M, const void* W,
+                                       const bi_gemm_scales* scales, void* y, void* stream) {
+  int rc = validate_run(h, x, M, W, scales, y);
+  if (rc != BI_GEMM_OK || M == 0) return rc;
+  std::lock_guard<std::mutex> lk(h->mu);
+  return launch(h, x, M, W, scales, y, static_cast<cudaStream_t>(stream), 0, 2u);
+}

@@ -869,7 +869,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (epi_tid == 0) {
           uint32_t* cnt = p.counters + sub;
           const uint32_t S = uint32_t(p.splits);
-          const uint32_t old = atomicAdd(cnt, 1u);
+          bool arrive = true;
+#ifdef BI_GEMM_CONTROLS
+          // control build only: split 0 never counts its arrival, so the others' waits expire
+          arrive = !((p.test_flags & 2u) && uc.s == 0);
+#endif
+          const uint32_t old = arrive ? atomicAdd(cnt, 1u) : 0u;
           uint32_t verdict = (old == S - 1) ? 1u : 0u;
           if (p.coop_merge) {
             // arrivals count 0 .. S; then departures S .. 2S, and the last one out resets the

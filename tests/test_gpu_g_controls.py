@@ -120,3 +120,24 @@ def test_stalled_split_run_recovers(ctl):
         y_ref, _, sabs = oracle.gemm_bf16(x, w, "f32")
         check_tolerance(host_bits(y), y_ref, sabs, oracle.TOL_F32, "split after timeout")
     L.bi_ctl_destroy(h)
+
+
+def test_shared_merge_wait_times_out_and_recovers(ctl):
+    """The split CTAs of a tile wait for each other before a shared merge; when one never
+    arrives the others' bounded waits expire, the run reports a timeout, and the next run (which
+    resets the arrival counters) is correct."""
+    K, N, M = 16384, 24, 100             # 32 resident split CTAs, 600 merge items: shared merge
+    x = ig.scaled_rows_bf16(73, M, K)
+    w = ig.normal_bf16(74, K, N, std=0.02)
+    xd, wd = dev_bf16(x), dev_bf16(w)
+    h = ctl.create(K, N, BI_BF16_OUT_F32, timeout_ns=50_000_000)
+    L, s = ctl.L, stream_ptr()
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    assert L.bi_ctl_run_skip_arrival(h, xd.data_ptr(), M, wd.data_ptr(), None, y.data_ptr(), s) == 0
+    assert L.bi_ctl_get_device_error(h, s) == BI_GEMM_ERR_TIMEOUT
+    y_ref, _, sabs = oracle.gemm_bf16(x, w, "f32")
+    for _ in range(2):
+        assert L.bi_ctl_run(h, xd.data_ptr(), M, wd.data_ptr(), None, y.data_ptr(), s) == 0
+        assert L.bi_ctl_get_device_error(h, s) == 0
+        check_tolerance(host_bits(y), y_ref, sabs, oracle.TOL_F32, "shared merge after timeout")
+    L.bi_ctl_destroy(h)
