@@ -59,9 +59,15 @@ def load_peaks():
 
 
 def kernel_hash():
+    """Hash of the kernel sources' code: comments and whitespace are dropped, so that editing a
+    comment does not invalidate a recorded profile."""
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        src = open(os.path.join(ROOT, f)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -5,14 +5,14 @@
 // Why this is batch invariant ("Batch-invariant matrix multiplication", nondeterminism
 // article: the three breakers are M-dependent split-K, stream-K and a smaller tensor-core
 // instruction at small M; the cure is one kernel configuration for every shape):
-//   * the output tile is always 128 x BN, the tcgen05 instruction always
-//     M=128 x N=BN x K=16 (bf16) or K=32 (MXFP8), whatever M is;
+//   * the output tile is always 128 x BN (256 x BN on a CTA pair), the tcgen05 instruction
+//     always M=128 (M=256 on a pair) x N=BN x K=16 (bf16) or K=32 (MXFP8), whatever M is;
 //   * every output element is reduced over k-blocks kb = 0 .. KB-1 in ascending order, and
 //     within a k-block over the same fixed sequence of MMA instructions;
 //   * a split count S > 1 is fixed when the handle is created (from K, N and the SM count,
-//     never M); split s always covers k-blocks [s*KB/S, (s+1)*KB/S), and the S fp32
-//     partials are merged in the fixed serial order ((p0 + p1) + p2) + ... by whichever
-//     CTA arrives last (an integer arrival counter; no floating-point atomics);
+//     never M); split s always covers the same k-blocks, and the S fp32 partials of every
+//     element are summed in the fixed serial order ((p0 + p1) + p2) + ..., whichever CTA does
+//     the sum (integer arrival counters; no floating-point atomics);
 //   * rows beyond M are zero-filled by TMA and never stored; a row's products never meet
 //     another row's, so neither M nor the other rows' contents can reach row i.
 // The persistent tile order (which SM computes which tile, and when) does change with M,
@@ -893,7 +893,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           *last_flag = verdict;
         }
-        // Hand-off 2: the verdict is visible to all four warps.
+        // Hand-off 2: the verdict is visible to all epilogue warps.
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(epi_bar);
         if (!warp_wait_phase(epi_bar, ephase, sc, kErrTimeoutEpilogue)) break;
