@@ -180,18 +180,14 @@ struct SyncCtx {
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the abort flag and the error
 // bit) once the time limit passes, or as soon as another role has aborted.
-// How a wait observes a barrier phase: acquire at CTA scope (default), acquire at cluster scope
-// (the phase completes with arrivals from the peer CTA), or relaxed (nothing is ordered around
-// the test, so loads the waiting thread has in flight stay in flight; the writes that follow a
-// relaxed wait depend on its outcome by control only).
-enum class Wait { kCta, kCluster, kRelaxed };
+// How a wait observes a barrier phase: acquire at CTA scope (default) or acquire at cluster
+// scope (the phase completes with arrivals from the peer CTA).
+enum class Wait { kCta, kCluster };
 
 template <Wait kW = Wait::kCta>
 __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
   if constexpr (kW == Wait::kCluster)
     return ptx::mbar_try_wait_cluster(bar, parity);
-  else if constexpr (kW == Wait::kRelaxed)
-    return ptx::mbar_try_wait_relaxed(bar, parity);
   else
     return ptx::mbar_try_wait(bar, parity);
 }
