@@ -53,7 +53,7 @@ int bi_ctl_run_stall(bi_gemm_t h, const void* x, int64_t M, const void* W,
                      const bi_gemm_scales* scales, void* y, void* stream);
 
 /* Failure injection for the shared split-K merge (used when every split unit has its own
- * resident CTA and a sub-tile has more than 256 merge items): split 0 of every tile never counts
+ * resident CTA and a sub-tile's partials exceed 24 KB): split 0 of every tile never counts
  * its arrival, so the other split CTAs' bounded waits for it expire.  The status word then reads
  * BI_GEMM_ERR_TIMEOUT; y is undefined; the next run resets the arrival counters. */
 int bi_ctl_run_skip_arrival(bi_gemm_t h, const void* x, int64_t M, const void* W,

@@ -33,7 +33,8 @@
 namespace bigemm {
 
 constexpr int kVersion = (1 << 16) | 0;
-constexpr int64_t kEpilogueThreads = 256;   // eight epilogue warps in every configuration
+constexpr int64_t kCoopMergeBytes = 24 << 10;   // partial bytes of a sub-tile above which its
+                                                // split CTAs share the merge
 constexpr uint64_t kDefaultTimeoutNs = 5ull * 1000 * 1000 * 1000;
 // Raster order (visiting order only; it decides no arithmetic): while x fits comfortably in L2
 // the M tiles vary fastest (x stays resident, W streams once); a larger x is visited in groups
@@ -302,11 +303,13 @@ int launch_core(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_ge
   const int64_t units = sh.tiles * split;
   const int groups = int(std::min<int64_t>(units, h->max_groups));
   // The split CTAs of a 128-row sub-tile share its merge when every unit has its own resident
-  // CTA group (so they can wait for each other) and the sub-tile has more (row, 4-column) items
-  // than one CTA's epilogue threads; otherwise the last CTA to arrive merges alone.  Either way
-  // every element is summed in split order, so this choice moves data, not arithmetic.
+  // CTA group (so they can wait for each other) and the partials of the sub-tile are more than
+  // one CTA reads faster than the S CTAs can meet (kCoopMergeBytes, measured on GB300);
+  // otherwise the last CTA to arrive merges alone.  Either way every element is summed in split
+  // order, so this choice moves data, not arithmetic.
   const int64_t merge_items = std::min<int64_t>(M, kBM) * ((std::min<int64_t>(h->N, h->kern.bn) + 3) / 4);
-  p.coop_merge = (split > 1 && units <= h->max_groups && merge_items > kEpilogueThreads) ? 1 : 0;
+  p.coop_merge =
+      (split > 1 && units <= h->max_groups && merge_items * split * 16 > kCoopMergeBytes) ? 1 : 0;
   void* args[4] = {&tmap_x, &h->tmap_w, &tmap_y, &p};
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));

@@ -68,8 +68,9 @@ struct KParams {
   int32_t kblocks;          // KB = ceil(K / BK)
   int32_t a_box_rows;       // rows per x TMA box: 128, or round_up(M, 8) when M < 128
   int32_t group_n;          // raster order: N tiles per group (M tiles vary fastest within it)
-  int32_t coop_merge;       // S > 1 and every unit has its own resident CTA group: the S split
-                            // CTAs of a sub-tile share its merge (else the last to arrive merges)
+  int32_t coop_merge;       // S > 1, every unit has its own resident CTA group and the merge is
+                            // large: the S split CTAs of a sub-tile share it (else the last to
+                            // arrive merges alone)
   uint64_t timeout_ns;
   uint32_t test_flags;      // only read by the control build
 };
@@ -127,7 +128,6 @@ struct KCfg {
   static_assert(!kRegSplit || EPI_WARP0 * 32 * REGS_LOW + EPI_WARPS * 32 * REGS_HIGH <= 65536,
                 "register split exceeds the launch's registers");
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-  static_assert(EPI_THREADS == 256, "the host's merge-sharing rule assumes 256 epilogue threads");
   static constexpr int THREADS = NUM_WARPS * 32;
   // TMEM columns: accumulators first, then 16 columns of scale factors per stage.
   static constexpr int SF_TMEM_COL0 = ACC_BUFS * BN;
@@ -856,13 +856,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // every unit has its own resident CTA group (coop_merge), the S split CTAs wait for one
         // another and each merges 1/S of the elements; otherwise the last CTA to arrive (an
         // integer counter) merges them all.
-        // Hand-off 1: every partial of this CTA is stored and fenced before the count.
-        __threadfence();
+        // Hand-off 1: every partial of this CTA is stored before the count.  The barrier makes the
+        // epilogue threads' stores visible to the counting thread, whose GPU-scope fence then
+        // publishes them (cumulatively) before its arrival.
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(epi_bar);
         if (!warp_wait_phase(epi_bar, ephase, sc, kErrTimeoutEpilogue)) break;
         ephase ^= 1u;
         if (epi_tid == 0) {
+          __threadfence();
           uint32_t* cnt = p.counters + sub;
           const uint32_t S = uint32_t(p.splits);
           bool arrive = true;
@@ -872,6 +874,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #endif
           const uint32_t old = arrive ? atomicAdd(cnt, 1u) : 0u;
           uint32_t verdict = (old == S - 1) ? 1u : 0u;
+          if (verdict) __threadfence();   // acquire: the other partials are visible before the merge
           if (p.coop_merge) {
             // arrivals count 0 .. S; then departures S .. 2S, and the last one out resets the
             // counter for the next launch (every CTA has seen S by then)
@@ -897,9 +900,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const bool merge = *last_flag != 0u;
         if (merge) {
           // (row, 4-column group) items, spread over the merging CTA(s)' epilogue threads, with
-          // the loads issued in independent batches (16, or 8 where the epilogue shares its
-          // register budget)
-          __threadfence();
+          // the loads of each item issued together (see below).  The counting thread acquired
+          // the partials (its fence after the last arrival, or its acquiring load of the full
+          // count) before hand-off 2.
           const int row0 = uc.m_tile * C::TILE_M + int(rank) * kBM;
           const int rows = min(kBM, p.M - row0);
           const int groups = (min(C::BN, p.N - col_tile0) + 3) / 4;
@@ -912,28 +915,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           const float* src0 = p.ws + ((size_t)sub * p.splits) * kBM * C::BN;
           const size_t sstride = (size_t)kBM * C::BN;
-#pragma unroll 1
-          for (int it = it_begin + epi_tid; it < it_end; it += C::EPI_THREADS) {
-            const int rr = it / groups, g4 = it - rr * groups;
-            const float* sp = src0 + (size_t)rr * C::BN + g4 * 4;
-            float4 acc = __ldcg(reinterpret_cast<const float4*>(sp));
-            constexpr int kMergeBatch = C::kRegSplit ? 8 : 16;   // loads in flight per item
-#pragma unroll 1
-            for (int s0 = 1; s0 < p.splits; s0 += kMergeBatch) {
-              float4 t[kMergeBatch];
-#pragma unroll
-              for (int j = 0; j < kMergeBatch; ++j)
-                if (s0 + j < p.splits) t[j] = __ldcg(reinterpret_cast<const float4*>(sp + (s0 + j) * sstride));
-#pragma unroll
-              for (int j = 0; j < kMergeBatch; ++j) {
-                if (s0 + j < p.splits) {
-                  acc.x = acc.x + t[j].x;
-                  acc.y = acc.y + t[j].y;
-                  acc.z = acc.z + t[j].z;
-                  acc.w = acc.w + t[j].w;
-                }
-              }
-            }
+          auto store_item = [&](int rr, int g4, const float4& acc) {
             const size_t yo = (size_t)(row0 + rr) * p.N + col_tile0 + g4 * 4;
             if constexpr (C::kOutF32) {
               *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + yo) = acc;
@@ -942,6 +924,69 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               pk.x = ptx::pack_bf16x2(acc.x, acc.y);
               pk.y = ptx::pack_bf16x2(acc.z, acc.w);
               *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.y) + yo) = pk;
+            }
+          };
+          // The epilogue's staging buffers are idle in a split run (partials go straight to
+          // global memory): each merging thread copies all S partials of its item into its own
+          // slot there with cp.async, so that they arrive in one round trip, then sums them.
+          // Slots are padded by 16 bytes so that the threads' reads spread over the banks.
+          constexpr int kStgTotal = C::EPI_WARPS * C::STG_BUFS * C::STG_BYTES;
+          const int slot_bytes = p.splits * 16 + 16;
+          const int per_round = min(C::EPI_THREADS, kStgTotal / slot_bytes);
+          if (per_round >= 1) {
+            const uint32_t slot = sbase + C::OFF_STG + uint32_t(epi_tid * slot_bytes);
+#pragma unroll 1
+            for (int base = it_begin; base < it_end; base += per_round) {
+              const int it = base + epi_tid;
+              if (epi_tid < per_round && it < it_end) {
+                const int rr = it / groups, g4 = it - rr * groups;
+                const float* sp = src0 + (size_t)rr * C::BN + g4 * 4;
+#pragma unroll 4
+                for (int s = 0; s < p.splits; ++s) ptx::cp_async_16(slot + s * 16, sp + s * sstride, 16u);
+                ptx::cp_async_commit();
+                ptx::cp_async_wait<0>();
+                float4 acc = ptx::ld_shared_f4(slot);
+#pragma unroll 4
+                for (int s = 1; s < p.splits; ++s) {
+                  const float4 t = ptx::ld_shared_f4(slot + s * 16);
+                  acc.x = acc.x + t.x;
+                  acc.y = acc.y + t.y;
+                  acc.z = acc.z + t.z;
+                  acc.w = acc.w + t.w;
+                }
+                store_item(rr, g4, acc);
+              }
+            }
+          } else {
+            // S too large for the staging: loads in registers, in batches
+#pragma unroll 1
+            for (int it = it_begin + epi_tid; it < it_end; it += C::EPI_THREADS) {
+              const int rr = it / groups, g4 = it - rr * groups;
+              const float* sp = src0 + (size_t)rr * C::BN + g4 * 4;
+              constexpr int kMergeBatch = C::kRegSplit ? 4 : 16;   // loads in flight per item
+              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+              for (int s0 = 0; s0 < p.splits; s0 += kMergeBatch) {
+                float4 t[kMergeBatch];
+#pragma unroll
+                for (int j = 0; j < kMergeBatch; ++j)
+                  if (s0 + j < p.splits) t[j] = __ldcg(reinterpret_cast<const float4*>(sp + (s0 + j) * sstride));
+                int j0 = 0;
+                if (s0 == 0) {                   // the sum starts from p0 itself, not 0 + p0
+                  acc = t[0];
+                  j0 = 1;
+                }
+#pragma unroll
+                for (int j = 0; j < kMergeBatch; ++j) {
+                  if (j >= j0 && s0 + j < p.splits) {
+                    acc.x = acc.x + t[j].x;
+                    acc.y = acc.y + t[j].y;
+                    acc.z = acc.z + t[j].z;
+                    acc.w = acc.w + t[j].w;
+                  }
+                }
+              }
+              store_item(rr, g4, acc);
             }
           }
           if (!p.coop_merge && epi_tid == 0) p.counters[sub] = 0u;   // ready for the next launch

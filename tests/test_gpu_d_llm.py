@@ -1,7 +1,8 @@
 """LLM projection sweep: bf16 x[M,4096]~N(0,1) · W[4096,14336]~N(0,0.02), bf16 out,
 M in {1,7,8,15,16,17,63,64,65,128,129,192,193,256} (the batch boundaries of "[BI][DSv4] Make
 mHC tilelang ops batch invariant", "Tests") extended to 512..8192.  Rows are compared
-bitwise across all M; sampled rows against the oracle; A/B cells at {0, mid, last}."""
+bitwise across all M; every element of the M = 64 launch and 64 sampled rows of the M = 8192
+launch against the oracle; A/B cells at {0, mid, last}."""
 import numpy as np
 import pytest
 import torch
@@ -19,10 +20,12 @@ MMAX = M_LIST[-1]
 
 
 def sample_rows():
+    """64 rows of the M = 8192 output: the tile and batch boundaries plus seeded rows."""
     rows = {0, 1, 6, 7, 8, 14, 15, 16, 62, 63, 64, 127, 128, 191, 192, 255, 511, 1023, 2047,
             4095, 4096, 8191}
     rng = np.random.default_rng(7)
-    rows |= set(int(r) for r in rng.integers(0, MMAX, 10))
+    while len(rows) < 64:
+        rows.add(int(rng.integers(0, MMAX)))
     return sorted(rows)
 
 
@@ -61,6 +64,16 @@ def test_parity_sampled_rows(setup):
     agree = float(np.mean(y == y_ref))
     print(f"LLM bf16 max ratio {worst:.3g}, bitwise agreement with oracle {agree:.4f}")
     assert agree > 0.99
+
+
+def test_parity_every_row_m64(setup):
+    """Every element of the M = 64 launch against the oracle (all 64 rows, all 14336 columns)."""
+    g, W, X, Wd, Xd, y_full = setup
+    y64 = host_bits(g(Xd[:64], Wd))
+    y_ref, _, sabs = oracle.gemm_bf16(X[:64], W, "bf16")
+    worst = check_tolerance(y64, y_ref, sabs, oracle.TOL_BF16, "LLM projection, M = 64")
+    print(f"LLM bf16 M=64 every element: max ratio {worst:.3g}, bitwise agreement "
+          f"{float(np.mean(y64 == y_ref)):.4f}")
 
 
 def test_bi_cells(setup):

@@ -126,7 +126,7 @@ def test_shared_merge_wait_times_out_and_recovers(ctl):
     """The split CTAs of a tile wait for each other before a shared merge; when one never
     arrives the others' bounded waits expire, the run reports a timeout, and the next run (which
     resets the arrival counters) is correct."""
-    K, N, M = 16384, 24, 100             # 32 resident split CTAs, 600 merge items: shared merge
+    K, N, M = 16384, 24, 100             # 32 resident split CTAs, 300 KB of partials: shared merge
     x = ig.scaled_rows_bf16(73, M, K)
     w = ig.normal_bf16(74, K, N, std=0.02)
     xd, wd = dev_bf16(x), dev_bf16(w)
