@@ -82,3 +82,22 @@ def test_merge_paths_give_identical_bits(setup, max_ctas):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (M, max_ctas)
     assert capped.device_error() == 0 and g.device_error() == 0
     capped.close()
+
+
+def test_split_too_large_for_merge_staging():
+    """A fixed split of 4096 k-ranges: one item's partials (64 KB) no longer fit the epilogue
+    staging, so the merge takes its register-batch path; still every element against the
+    oracle and rows bitwise equal across M."""
+    K, N, M = 262144, 24, 8
+    x = ig.scaled_rows_bf16(91, M, K)
+    w = ig.normal_bf16(92, K, N, std=0.02)
+    g = BiGemm(K, N, "bf16_f32", split_k=4096)
+    assert g.config["split_k"] == 4096
+    xd, wd = dev_bf16(x), dev_bf16(w)
+    y = host_bits(g(xd, wd))
+    y_ref, _, sabs = oracle.gemm_bf16(x, w, "f32")
+    check_tolerance(y, y_ref, sabs, oracle.TOL_F32, "S=4096")
+    y1 = host_bits(g(xd[3:4].contiguous(), wd))
+    assert np.array_equal(y1.view(np.uint32), y[3:4].view(np.uint32))
+    assert g.device_error() == 0
+    g.close()

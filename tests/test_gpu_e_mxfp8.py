@@ -125,3 +125,20 @@ def test_mxfp8_ragged_and_split(K, N, M, split):
             assert torch.equal(y2.view(torch.int16), y[:M2].view(torch.int16)), M2
     assert g.device_error() == 0
     g.close()
+
+
+def test_mxfp8_pair_split_too_large_for_merge_staging():
+    """MXFP8 on the CTA-pair tile with a fixed split of 1024: one item's partials exceed the
+    epilogue staging, so the merge takes its register-batch path."""
+    K, N, M = 131072, 256, 8
+    x, sx, w, sw = inputs(K, N, ("VAR", "VAR"), rows=M)
+    g = BiGemm(K, N, "mxfp8", split_k=1024)
+    assert g.config["split_k"] == 1024 and g.config["ctas_per_tile"] == 2
+    xd, sxd, wd, swd = dev_u8(x), dev_u8(sx), dev_u8(w), dev_u8(sw)
+    y = g(xd, wd, sx=sxd, sw=swd)
+    y_ref, _, sabs = oracle.gemm_mxfp8(x, sx, w, sw)
+    check_tolerance(host_bits(y), y_ref, sabs, oracle.TOL_BF16, "MXFP8 S=1024")
+    y1 = g(xd[5:6], wd, sx=sxd[5:6], sw=swd)
+    assert torch.equal(y1.view(torch.int16), y[5:6].view(torch.int16))
+    assert g.device_error() == 0
+    g.close()
