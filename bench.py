@@ -146,13 +146,20 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ distributed
 
+_BACKEND = None
+
+
 def dist_init():
+    """Join the process group when launched with WORLD_SIZE > 1 (one rank per GPU, NCCL; gloo
+    without GPUs or when BI_DIST_BACKEND says so).  Returns (rank, world, local rank)."""
+    global _BACKEND
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl" if _cuda() else "gloo")
+        _BACKEND = os.environ.get("BI_DIST_BACKEND") or ("nccl" if _cuda() else "gloo")
+        dist.init_process_group(_BACKEND)
     return rank, world, local
 
 
@@ -172,7 +179,7 @@ def max_over_ranks(v, world):
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda" if _cuda() else "cpu")
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if _BACKEND == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
