@@ -185,3 +185,9 @@ def target_rows(m: int) -> list[int]:
         if r not in out:
             out.append(r)
     return out
+
+
+def rmsnorm_weight_bf16(seed: int, d: int) -> np.ndarray:
+    """RMSNorm weight g[d]: 1 + 0.1 * N(0, 1), rounded to bf16 (weights of a trained norm sit
+    near 1; the pages give no distribution)."""
+    return to_bf16_bits(1.0 + 0.1 * normal(seed, 0, d))

@@ -1,4 +1,4 @@
-"""CPU oracle for the batch-invariant GEMM y = x·W — TEST INFRASTRUCTURE.
+"""CPU oracle for the batch-invariant GEMM y = x·W and RMSNorm — TEST INFRASTRUCTURE.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may
 import this package.  The product (``invariant_bi_gemm_gb300``) never does, and the
@@ -12,6 +12,10 @@ article; the row-wise definition y[i] = f(x[i], W) of the batch-invariance issue
 
 with a single round-to-nearest-even to the output dtype, and the absolute sum
 S_abs[i, j] = sum_k |dec(x[i, k]) * dec(w[k, j])| returned for the tolerance.
+
+RMSNorm ("Batch-invariant RMSNorm", nondeterminism article): for each row,
+v[i, j] = (x[i, j] / sqrt(sum_{j ascending} x[i, j]^2 / d + eps)) * g[j] in fp64,
+rounded once to bf16; v is returned for the tolerance.
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against exact
 rational arithmetic, the pages' worked examples and identities, and library
@@ -56,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.bio_gemm_bf16.restype = ctypes.c_int
         L.bio_gemm_mxfp8.argtypes = [P, P, I64, I64, P, P, I64, P, I64, P, P, P]
         L.bio_gemm_mxfp8.restype = ctypes.c_int
+        L.bio_rmsnorm_bf16.argtypes = [P, I64, I64, P, ctypes.c_double, P, I64, P, P]
+        L.bio_rmsnorm_bf16.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -139,6 +145,25 @@ def gemm_mxfp8(x, sx, w, sw, rows=None):
     return y, acc, sabs
 
 
+def rmsnorm_bf16(x: np.ndarray, g: np.ndarray, eps: float, rows=None):
+    """RMSNorm of bf16 rows ("Batch-invariant RMSNorm", nondeterminism article).
+
+    x uint16[M, d], g uint16[d] (bf16 patterns), eps the fp32 value the GPU adds, passed as
+    a double.  Returns (y uint16 bf16 patterns [R, d], v fp64 [R, d] unrounded).
+    """
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    g = np.ascontiguousarray(g, dtype=np.uint16)
+    M, d = x.shape
+    assert g.shape == (d,)
+    r, R = _rows_arg(rows, M)
+    y = np.empty((R, d), np.uint16)
+    v = np.empty((R, d), np.float64)
+    rc = lib().bio_rmsnorm_bf16(_ptr(x), M, d, _ptr(g), float(eps), _ptr(r), R, _ptr(y), _ptr(v))
+    if rc:
+        raise ValueError("bio_rmsnorm_bf16 rejected its arguments")
+    return y, v
+
+
 def bf16_to_f64(b) -> float:
     return lib().bio_bf16_to_f64(int(b))
 
@@ -181,7 +206,15 @@ def tolerance_violations(y_gpu_f64: np.ndarray, y_ref_f64: np.ndarray, sabs: np.
     return int(bad.sum()), float(np.nanmax(ratio)) if ratio.size else 0.0
 
 
+# RMSNorm (bf16 out): |y - v| <= (2^-8 + 2^-16) * |v| with v the oracle's unrounded fp64
+# value.  2^-8 is the bf16 rounding of the output; 2^-16 bounds the relative error of the fp32
+# computation before that rounding (sum of at most 136 positive squares, one division, one
+# reciprocal square root of at most 2 ulp, two products: below 1e-5 for d <= 16384).
+TOL_RMSNORM_REL = 2.0**-8 + 2.0**-16
+
+
 __all__ = [
+    "rmsnorm_bf16", "TOL_RMSNORM_REL",
     "gemm_f64", "gemm_bf16", "gemm_mxfp8", "bf16_to_f64", "e4m3_to_f64", "e8m0_to_f64",
     "f64_to_bf16", "f64_to_f32_bits", "bf16_array_to_f64", "TOL_BF16", "TOL_F32",
     "tolerance_violations", "lib",

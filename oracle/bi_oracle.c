@@ -1,5 +1,5 @@
 /*
- * bi_oracle.c — plain CPU oracle for the batch-invariant GEMM (TEST INFRASTRUCTURE).
+ * bi_oracle.c — plain CPU oracle for the batch-invariant GEMM and RMSNorm (TEST INFRASTRUCTURE).
  *
  * Only tests, the smoke check and the benchmark's CPU-baseline leg use this file.
  * It follows the plain definition C_ij = sum_k A_ik B_kj of the nondeterminism
@@ -199,5 +199,37 @@ int bio_gemm_mxfp8(const uint8_t* x, const uint8_t* sx, int64_t M, int64_t K,
     }
     free(a);
     free(s);
+    return 0;
+}
+
+/* ---------------------------------------------------------------- RMSNorm */
+
+/* One row at a time, straight from the definition ("Batch-invariant RMSNorm", nondeterminism
+ * article): the sum of squares in ascending j, the mean, the reciprocal square root, then
+ * each element times it and times its weight, all in fp64, with one rounding to bf16. */
+int bio_rmsnorm_bf16(const uint16_t* x, int64_t M, int64_t d, const uint16_t* g, double eps,
+                     const int64_t* rows, int64_t nrows, uint16_t* y, double* v) {
+    if (M < 0 || d < 0 || !(eps >= 0.0)) return -1;
+    int64_t R = rows ? nrows : M;
+    if (R < 0) return -1;
+    if (R > 0 && d == 0) return -1;
+    if (R > 0 && (!x || !g || !y)) return -1;
+    for (int64_t r = 0; r < R; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= M) return -1;
+        const uint16_t* xr = x + i * d;
+        double ss = 0.0;
+        for (int64_t j = 0; j < d; ++j) {
+            const double xv = bio_bf16_to_f64(xr[j]);
+            ss = ss + xv * xv;
+        }
+        const double ms = ss / (double)d;
+        const double rr = 1.0 / sqrt(ms + eps);
+        for (int64_t j = 0; j < d; ++j) {
+            const double val = (bio_bf16_to_f64(xr[j]) * rr) * bio_bf16_to_f64(g[j]);
+            y[r * d + j] = bio_f64_to_bf16(val);
+            if (v) v[r * d + j] = val;
+        }
+    }
     return 0;
 }

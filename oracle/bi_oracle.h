@@ -1,5 +1,6 @@
 /*
- * bi_oracle.h — plain, slow CPU oracle for the batch-invariant GEMM y = x·W.
+ * bi_oracle.h — plain, slow CPU oracle for the batch-invariant GEMM y = x·W
+ * (and the batch-invariant RMSNorm, declared at the end).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
  * CPU-baseline leg may load this library.  The product path (the CUDA library and
@@ -63,6 +64,22 @@ int bio_gemm_bf16(const uint16_t* x, int64_t M, int64_t K, const uint16_t* w, in
 int bio_gemm_mxfp8(const uint8_t* x, const uint8_t* sx, int64_t M, int64_t K,
                    const uint8_t* w, const uint8_t* sw, int64_t N,
                    const int64_t* rows, int64_t nrows, uint16_t* y, double* acc, double* sabs);
+
+/* RMSNorm of bf16 rows ("Batch-invariant RMSNorm", nondeterminism article: RMSNorm(x_i) =
+ * x_i / sqrt(mean_j x_ij^2 + eps) * gamma, one reduction along the feature axis per row):
+ *
+ *     ms[i]   = (sum_{j=0..d-1, ascending} x[i,j]^2) / d          (fp64)
+ *     r[i]    = 1 / sqrt(ms[i] + eps)                              (fp64)
+ *     v[i,j]  = (x[i,j] * r[i]) * g[j]                             (fp64, the article's order
+ *                                                                   x * rsqrt(mean) * weight)
+ *     y[i,j]  = RNE bf16 of v[i,j]
+ *
+ * x[M,d] and y bf16 patterns row-major, g[d] bf16 patterns.  rows/nrows select rows as for
+ * bio_gemm_bf16.  v (fp64, same packing as y) may be NULL; it is the unrounded value the
+ * tolerance is measured against.  Returns -1 on a bad argument (negative sizes, d = 0 with
+ * M > 0, NaN or negative eps). */
+int bio_rmsnorm_bf16(const uint16_t* x, int64_t M, int64_t d, const uint16_t* g, double eps,
+                     const int64_t* rows, int64_t nrows, uint16_t* y, double* v);
 
 #ifdef __cplusplus
 }

@@ -122,3 +122,26 @@ def gamma(n: int, u: float) -> float:
     nu = n * u
     assert nu < 1
     return nu / (1 - nu)
+
+
+def bf16_bits_of_signed_sqrt(q: Fraction, negative: bool) -> int:
+    """Bits of RNE_bf16(+-sqrt(q)) for a rational q >= 0, decided exactly: the result r is the
+    bf16 value whose rounding interval [mid(r-, r), mid(r, r+)] holds sqrt(q), tested by
+    comparing q with the squared midpoints (ties go to the even pattern).  Finite normal
+    results only (the tests keep their values inside the bf16 normal range)."""
+    assert q >= 0
+    sb = 0x8000 if negative else 0
+    if q == 0:
+        return sb
+    b = to_bf16_bits_exact(Fraction(float(q) ** 0.5)) & 0x7FFF    # first guess, then fix up
+    assert 0x0080 <= b < 0x7F80
+    while True:
+        v = bf16_value(b)
+        lo = (bf16_value(b - 1) + v) / 2
+        hi = (v + bf16_value(b + 1)) / 2
+        if q < lo * lo or (q == lo * lo and b % 2 == 1):
+            b -= 1
+        elif q > hi * hi or (q == hi * hi and b % 2 == 1):
+            b += 1
+        else:
+            return sb | b
