@@ -558,7 +558,95 @@ def measure_other_paths(dev, peaks):
     out["linspace_2048x4096x4096_f32"] = {"us": round(t * 1e6, 2), "tflops": round(flops(2048, 4096, 4096) / t / 1e12, 1),
                                           "frac_tensor": round(flops(2048, 4096, 4096) / t / 1e12 / peaks["bf16_tflops"], 3)}
     g.close()
+    out["rmsnorm"] = measure_rmsnorm(dev, peaks, bf)
     return out
+
+
+RMS_D = 4096
+RMS_EPS = 1e-6
+
+
+def rmsnorm_bytes(M, d=RMS_D):
+    """Algorithmic HBM bytes of one RMSNorm launch: x read once, y written once, the weight."""
+    return 2 * M * d + 2 * M * d + 2 * d
+
+
+def measure_rmsnorm(dev, peaks, bf):
+    """Batch-invariant RMSNorm of bf16 rows, d = 4096 (the LLM projection's K), graph-timed with
+    rotating (x, y) sets whose total exceeds twice the L2, so every launch reads cold rows."""
+    import numpy as np
+    import torch
+    import inputgen as ig
+    from invariant_bi_gemm_gb300 import BiRmsNorm
+
+    n = BiRmsNorm(RMS_D, RMS_EPS)
+    gw = bf(ig.rmsnorm_weight_bf16(ig.SEED_W, RMS_D))
+    base = bf(ig.scaled_rows_bf16(ig.SEED_X, 8192, RMS_D))
+    rows = []
+    for M in (1, 64, 256, 2048, 8192, 32768):
+        per_set = 4 * M * RMS_D
+        nsets = max(3, min(64, int(2 * 256e6 // per_set) + 1))
+        xs = [base.repeat((M + 8191) // 8192, 1)[:M].contiguous() for _ in range(nsets)]
+        ys = [torch.empty_like(x) for x in xs]
+        reps = nsets * max(1, 30 // nsets)
+        for i in range(3):
+            n(xs[i % nsets], gw, ys[i % nsets])
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for i in range(reps):
+                n(xs[i % nsets], gw, ys[i % nsets])
+        gr.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            gr.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) / reps / 1e3)
+        t = statistics.median(ts)
+        by = rmsnorm_bytes(M)
+        rows.append({"M": M, "us": round(t * 1e6, 2), "gbs": round(by / t / 1e9, 1),
+                     "frac_hbm": round(by / t / 1e9 / peaks["hbm_gbs"], 3)})
+        del xs, ys, gr
+    cfg = n.config
+    n.close()
+    return {"shape": f"bf16 x[M,{RMS_D}] -> y[M,{RMS_D}], weight [{RMS_D}], eps {RMS_EPS}",
+            "threads_per_row": cfg["threads"], "grid_bound": cfg["max_ctas"], "rows": rows,
+            "bytes": "2Md (x) + 2Md (y) + 2d (weight)",
+            "note": "graph-timed; rotating (x, y) sets > 2x L2 for every M; small M is launch-latency-bound"}
+
+
+def run_rmsnorm_only(args):
+    """Launch only the RMSNorm (d = 4096) at one M, eagerly: --warmup + --steps launches.  For
+    profiling; prints the average launch time as one JSON line (not the benchmark line)."""
+    import numpy as np
+    import torch
+
+    import inputgen as ig
+    from invariant_bi_gemm_gb300 import BiRmsNorm
+
+    dev = torch.device("cuda", 0)
+    M = args.rmsnorm_only_m
+    x = torch.from_numpy(ig.scaled_rows_bf16(ig.SEED_X, M, RMS_D).view(np.int16)).to(dev).view(torch.bfloat16)
+    gw = torch.from_numpy(ig.rmsnorm_weight_bf16(ig.SEED_W, RMS_D).view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty_like(x)
+    n = BiRmsNorm(RMS_D, RMS_EPS)
+    for _ in range(args.warmup):
+        n(x, gw, y)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        n(x, gw, y)
+    b.record()
+    torch.cuda.synchronize()
+    t = a.elapsed_time(b) / 1e3 / max(1, args.steps)
+    print(json.dumps({"rmsnorm_only_m": M, "d": RMS_D, "us_per_launch": round(t * 1e6, 2),
+                      "gbs": round(rmsnorm_bytes(M) / t / 1e9, 1)}))
+    n.close()
 
 
 def run_mxfp8_only(args):
@@ -607,11 +695,16 @@ def main():
     ap.add_argument("--no-paths", action="store_true")
     ap.add_argument("--only-m", type=int, default=0,
                     help="time a single M of the sweep only (for profiling); skips e2e, paths, CPU")
+    ap.add_argument("--rmsnorm-only-m", type=int, default=0,
+                    help="profiling aid: launch only the RMSNorm (d = 4096) at this M, eagerly, and exit")
     ap.add_argument("--mxfp8-only-m", type=int, default=0,
                     help="launch only the MXFP8 LLM-shape GEMM at this M (for profiling)")
     args = ap.parse_args()
     if args.mxfp8_only_m:
         run_mxfp8_only(args)
+        return
+    if args.rmsnorm_only_m:
+        run_rmsnorm_only(args)
         return
     if args.only_m:
         global M_SWEEP

@@ -59,6 +59,14 @@ int bi_ctl_run_stall(bi_gemm_t h, const void* x, int64_t M, const void* W,
 int bi_ctl_run_skip_arrival(bi_gemm_t h, const void* x, int64_t M, const void* W,
                             const bi_gemm_scales* scales, void* y, void* stream);
 
+/* Control N3 (RMSNorm of bf16 rows, include/bi_rmsnorm.h, written in fp32 before the bf16
+ * rounding so that any change in the reduction order shows).  mkeyed = 0: the product's threads
+ * per row, fixed from d (must be batch-invariant).  mkeyed = 1: threads per row chosen from the
+ * batch size, 1024 while M <= 16 and the product's count above (must not be).  x, g bf16 and y
+ * fp32 [M, d] device pointers, 16-byte aligned; codes as bi_rmsnorm_run. */
+int bi_ctl_rmsnorm_f32(const void* x, int64_t M, int64_t d, const void* g, float eps, void* y,
+                       int32_t mkeyed, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

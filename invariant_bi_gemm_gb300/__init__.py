@@ -1,13 +1,15 @@
-"""Python binding of the batch-invariant GEMM library (libbi_gemm.so, C ABI in include/bi_gemm.h).
+"""Python binding of the batch-invariant GEMM library (libbi_gemm.so, C ABI in include/bi_gemm.h
+and include/bi_rmsnorm.h).
 
-Argument marshalling only: every step of y = x·W runs in the CUDA kernels of
+Argument marshalling only: every step of y = x·W (and of the RMSNorm) runs in the CUDA kernels of
 ``csrc/``.  PyTorch supplies device memory and streams.  There is no CPU or
 PyTorch fallback: importing this module fails if the library has not been built
 (``python -m invariant_bi_gemm_gb300.build``), and every call that the library
 refuses raises ``BiGemmError``.
 
-Low-level functions carry the C names (``bi_gemm_create``, ``bi_gemm_run``, ...)
-and take raw device pointers; ``BiGemm`` wraps them for torch tensors.
+Low-level functions carry the C names (``bi_gemm_create``, ``bi_gemm_run``, ...,
+``bi_rmsnorm_run``) and take raw device pointers; ``BiGemm`` and ``BiRmsNorm`` wrap them
+for torch tensors.
 """
 from __future__ import annotations
 
@@ -37,6 +39,8 @@ EXPORTED_SYMBOLS = (
     "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_strerror",
     "bi_gemm_version", "bi_gemm_run_noalloc",
 )
+# every symbol include/bi_rmsnorm.h declares
+RMSNORM_EXPORTED_SYMBOLS = ("bi_rmsnorm_create", "bi_rmsnorm_run", "bi_rmsnorm_get_config", "bi_rmsnorm_destroy")
 
 
 class BiGemmError(RuntimeError):
@@ -59,6 +63,10 @@ class bi_gemm_config(ctypes.Structure):
         "num_sms", "max_ctas", "threads", "smem_bytes", "tmem_cols", "ctas_per_tile", "max_groups")]
 
 
+class bi_rmsnorm_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("d", "threads", "vectors_per_thread", "max_ctas", "num_sms")]
+
+
 def _load() -> ctypes.CDLL:
     path = _build.lib_path("libbi_gemm.so")
     if not os.path.exists(path):
@@ -78,8 +86,12 @@ def _load() -> ctypes.CDLL:
     L.bi_gemm_strerror.argtypes = [I32]
     L.bi_gemm_strerror.restype = ctypes.c_char_p
     L.bi_gemm_version.argtypes = []
+    L.bi_rmsnorm_create.argtypes = [ctypes.POINTER(P), I64, ctypes.c_float]
+    L.bi_rmsnorm_run.argtypes = [P, P, I64, P, P, P]
+    L.bi_rmsnorm_get_config.argtypes = [P, ctypes.POINTER(bi_rmsnorm_config)]
+    L.bi_rmsnorm_destroy.argtypes = [P]
     for n in ("bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_run_noalloc", "bi_gemm_get_device_error",
-              "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_version"):
+              "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_version") + RMSNORM_EXPORTED_SYMBOLS:
         getattr(L, n).restype = I32
     return L
 
@@ -163,7 +175,31 @@ def bi_gemm_workspace_size(h: int, M: int) -> int:
     return b.value
 
 
-# --------------------------------------------------------------------- torch wrapper
+def bi_rmsnorm_create(d: int, eps: float) -> int:
+    """Returns the handle (an opaque integer); raises BiGemmError on refusal."""
+    h = ctypes.c_void_p()
+    _check(library().bi_rmsnorm_create(ctypes.byref(h), int(d), float(eps)), "bi_rmsnorm_create")
+    return h.value
+
+
+def bi_rmsnorm_run(h: int, x: int, M: int, g: int, y: int, stream: int) -> None:
+    """Raw-pointer call: x, g, y device addresses, stream a cudaStream_t value."""
+    rc = library().bi_rmsnorm_run(ctypes.c_void_p(h), ctypes.c_void_p(x), int(M), ctypes.c_void_p(g),
+                                  ctypes.c_void_p(y), ctypes.c_void_p(stream))
+    _check(rc, "bi_rmsnorm_run")
+
+
+def bi_rmsnorm_get_config(h: int) -> dict:
+    c = bi_rmsnorm_config()
+    _check(library().bi_rmsnorm_get_config(ctypes.c_void_p(h), ctypes.byref(c)), "bi_rmsnorm_get_config")
+    return {n: getattr(c, n) for n, _ in bi_rmsnorm_config._fields_}
+
+
+def bi_rmsnorm_destroy(h: int) -> None:
+    _check(library().bi_rmsnorm_destroy(ctypes.c_void_p(h)), "bi_rmsnorm_destroy")
+
+
+# --------------------------------------------------------------------- torch wrappers
 
 _DTYPES = {"bf16": BI_BF16_OUT_BF16, "bf16_f32": BI_BF16_OUT_F32, "mxfp8": BI_MXFP8E4M3_OUT_BF16}
 
@@ -247,7 +283,53 @@ class BiGemm:
             pass
 
 
+class BiRmsNorm:
+    """y = RMSNorm(x) * g over rows of length d on torch bf16 tensors (x [M, d], g [d])."""
+
+    def __init__(self, d: int, eps: float = 1e-6):
+        self.d, self.eps = int(d), float(eps)
+        self.handle = bi_rmsnorm_create(self.d, self.eps)
+
+    @property
+    def config(self) -> dict:
+        return bi_rmsnorm_get_config(self.handle)
+
+    def run(self, x, g, y=None, stream=None):
+        import torch
+        if x.dim() != 2 or x.shape[1] != self.d or tuple(g.shape) != (self.d,):
+            raise ValueError("shape mismatch: x [M, d], g [d] expected")
+        if x.dtype != torch.bfloat16 or g.dtype != torch.bfloat16:
+            raise ValueError("bf16 inputs expected")
+        if not (x.is_cuda and g.is_cuda and x.is_contiguous() and g.is_contiguous()):
+            raise ValueError("x and g must be contiguous CUDA tensors")
+        M = int(x.shape[0])
+        if y is None:
+            y = torch.empty((M, self.d), dtype=torch.bfloat16, device=x.device)
+        if tuple(y.shape) != (M, self.d) or y.dtype != torch.bfloat16 or not y.is_contiguous():
+            raise ValueError("y must be a contiguous [M, d] bf16 tensor")
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        bi_rmsnorm_run(self.handle, x.data_ptr(), M, g.data_ptr(), y.data_ptr(), s)
+        return y
+
+    __call__ = run
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            bi_rmsnorm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 __all__ = [
+    "BiRmsNorm", "bi_rmsnorm_create", "bi_rmsnorm_run", "bi_rmsnorm_get_config", "bi_rmsnorm_destroy",
+    "bi_rmsnorm_config", "RMSNORM_EXPORTED_SYMBOLS",
     "BiGemm", "BiGemmError", "bi_gemm_create", "bi_gemm_run", "bi_gemm_run_noalloc", "bi_gemm_get_device_error",
     "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_strerror",
     "bi_gemm_version", "bi_gemm_scales", "bi_gemm_options", "EXPORTED_SYMBOLS", "LIB_PATH", "library",

@@ -1,7 +1,7 @@
 """Build the CUDA libraries in-tree with nvcc for sm_103a.
 
 Produces, under ``invariant_bi_gemm_gb300/_build/``:
-  libbi_gemm.so           the product (C ABI of include/bi_gemm.h)
+  libbi_gemm.so           the product (C ABI of include/bi_gemm.h and include/bi_rmsnorm.h)
   libbi_gemm_controls.so  test-only negative controls and failure injection
 
 Both are compiled in parallel; a library is rebuilt when any source is newer.
@@ -21,8 +21,8 @@ OUT = os.path.join(PKG, "_build")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 TARGETS = {
-    "libbi_gemm.so": "bi_gemm.cu",
-    "libbi_gemm_controls.so": "bi_gemm_controls.cu",
+    "libbi_gemm.so": ("bi_gemm.cu", "bi_rmsnorm.cu"),
+    "libbi_gemm_controls.so": ("bi_gemm_controls.cu",),
 }
 
 
@@ -50,7 +50,7 @@ def build(force: bool = False, verbose: bool = False) -> dict:
     """Compile every stale library; returns {name: path}.  Raises on a compiler error."""
     os.makedirs(OUT, exist_ok=True)
     procs = []
-    for name, src in TARGETS.items():
+    for name, srcs in TARGETS.items():
         out = lib_path(name)
         if not force and not _stale(out):
             continue
@@ -59,7 +59,7 @@ def build(force: bool = False, verbose: bool = False) -> dict:
             nvcc(), "-std=c++17", "-O3", ARCH, "-lineinfo",
             "-Xcompiler", "-fPIC,-fvisibility=hidden",
             "-Xlinker", "-Bsymbolic",
-            "-shared", "-o", tmp, os.path.join(CSRC, src),
+            "-shared", "-o", tmp, *[os.path.join(CSRC, s) for s in srcs],
         ]
         if verbose:
             cmd.insert(4, "-Xptxas=-v")

@@ -13,6 +13,7 @@
 #define BI_GEMM_CONTROLS 1
 #define BI_GEMM_API extern "C" __attribute__((visibility("hidden")))
 #include "bi_gemm.cu"
+#include "bi_rmsnorm.cu"
 
 #include <cuda_bf16.h>
 
@@ -120,4 +121,32 @@ BI_CTL_API int bi_ctl_run_skip_arrival(bi_gemm_t h, const void* x, int64_t M, co
   if (rc != BI_GEMM_OK || M == 0) return rc;
   std::lock_guard<std::mutex> lk(h->mu);
   return launch(h, x, M, W, scales, y, static_cast<cudaStream_t>(stream), 0, 2u);
+}
+
+// Control N3 (RMSNorm): fp32 output (the values before the bf16 rounding, so that any change of
+// reduction order shows) with the threads per row either fixed from d, the product's rule
+// (mkeyed = 0), or chosen from the batch size as a library keyed on occupancy would: 1024 threads
+// per row while M <= 16, 128 above (mkeyed = 1; a different butterfly and warp order).
+BI_CTL_API int bi_ctl_rmsnorm_f32(const void* x, int64_t M, int64_t d, const void* g, float eps, void* y,
+                                  int32_t mkeyed, void* stream) {
+  if (M < 0 || !birms::valid_d(d) || !(eps >= 0.0f)) return BI_GEMM_ERR_INVALID_ARG;
+  if (M == 0) return BI_GEMM_OK;
+  if (!x || !g || !y) return BI_GEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(y)) & 15u)
+    return BI_GEMM_ERR_ALIGNMENT;
+  const int nvec = int(d / birms::kVecElems);
+  int threads = birms::threads_for(d);
+  if (mkeyed) threads = std::max(threads, M <= 16 ? birms::kMaxThreads : birms::kMinThreads);
+  if (nvec > threads * birms::kVecsPerThread) return BI_GEMM_ERR_UNSUPPORTED;
+  birms::Params p;
+  p.x = static_cast<const uint4*>(x);
+  p.g = static_cast<const uint4*>(g);
+  p.y = y;
+  p.M = M;
+  p.nvec = nvec;
+  p.d = float(d);
+  p.eps = eps;
+  const unsigned grid = unsigned(std::min<int64_t>(M, 1024));
+  birms::rmsnorm_kernel<true><<<grid, unsigned(threads), 0, static_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? BI_GEMM_OK : BI_GEMM_ERR_CUDA;
 }

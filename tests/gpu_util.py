@@ -91,9 +91,10 @@ class Controls:
         L.bi_ctl_run_smallm_fork.argtypes = [P, P, I64, P, P, P]
         L.bi_ctl_run_stall.argtypes = [P, P, I64, P, P, P, P]
         L.bi_ctl_run_skip_arrival.argtypes = [P, P, I64, P, P, P, P]
+        L.bi_ctl_rmsnorm_f32.argtypes = [P, I64, I64, P, ctypes.c_float, P, ctypes.c_int32, P]
         for n in ("bi_ctl_create", "bi_ctl_destroy", "bi_ctl_get_device_error", "bi_ctl_run",
                   "bi_ctl_msplit_count", "bi_ctl_run_msplit", "bi_ctl_run_smallm_fork", "bi_ctl_run_stall",
-                  "bi_ctl_run_skip_arrival"):
+                  "bi_ctl_run_skip_arrival", "bi_ctl_rmsnorm_f32"):
             getattr(L, n).restype = I32
         self.L = L
 

@@ -27,6 +27,38 @@ def test_header_symbols_exported():
         assert hasattr(L, name), name
 
 
+def test_rmsnorm_header_symbols_exported():
+    declared = _declared("bi_rmsnorm.h")
+    assert set(declared) == set(bg.RMSNORM_EXPORTED_SYMBOLS)
+    L = ctypes.CDLL(bgbuild.lib_path("libbi_gemm.so"))
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+@pytest.mark.parametrize("d,eps,want", [
+    (4096, -1.0, bg.BI_GEMM_ERR_INVALID_ARG),
+    (4096, float("nan"), bg.BI_GEMM_ERR_INVALID_ARG),
+    (4096, float("inf"), bg.BI_GEMM_ERR_INVALID_ARG),
+    (0, 1e-6, bg.BI_GEMM_ERR_UNSUPPORTED),
+    (4, 1e-6, bg.BI_GEMM_ERR_UNSUPPORTED),
+    (4100, 1e-6, bg.BI_GEMM_ERR_UNSUPPORTED),          # row not a whole number of 16-byte vectors
+    (32776, 1e-6, bg.BI_GEMM_ERR_UNSUPPORTED),         # past 1024 threads x 4 vectors x 8
+    (-8, 1e-6, bg.BI_GEMM_ERR_UNSUPPORTED),
+])
+def test_rmsnorm_create_refuses_before_touching_cuda(d, eps, want):
+    h = ctypes.c_void_p()
+    assert bg.library().bi_rmsnorm_create(ctypes.byref(h), d, eps) == want
+    assert h.value is None
+
+
+def test_rmsnorm_null_arguments():
+    L = bg.library()
+    assert L.bi_rmsnorm_create(None, 4096, 1e-6) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_rmsnorm_run(None, None, 4, None, None, None) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_rmsnorm_get_config(None, None) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_rmsnorm_destroy(None) == bg.BI_GEMM_OK
+
+
 def test_controls_symbols_exported():
     declared = _declared("bi_gemm_controls.h")
     assert declared, "controls header declares nothing"
