@@ -191,3 +191,45 @@ def rmsnorm_weight_bf16(seed: int, d: int) -> np.ndarray:
     """RMSNorm weight g[d]: 1 + 0.1 * N(0, 1), rounded to bf16 (weights of a trained norm sit
     near 1; the pages give no distribution)."""
     return to_bf16_bits(1.0 + 0.1 * normal(seed, 0, d))
+
+
+# ----------------------------------------------------------------------------- attention inputs
+
+def kv_rows_bf16(seed: int, req: int, length: int, heads: int, dim: int, which: int) -> np.ndarray:
+    """Keys (which = 0) or values (which = 1) of one request, [length, heads, dim] bf16 ~ N(0, 1).
+    Element (j, h, i) is stream element ((j * heads + h) * dim + i) of the request's own stream,
+    so a request's content does not depend on its batch, its index or where its pages sit."""
+    s = (seed * 1_000_003 + req * 7_919 + which * 104_729) & 0xFFFFFFFF
+    return to_bf16_bits(normal(s, 0, length * heads * dim)).reshape(length, heads, dim)
+
+
+def query_bf16(seed: int, req: int, pos: int, heads: int, dim: int) -> np.ndarray:
+    """Query of request `req` at position `pos`, [heads, dim] bf16 ~ N(0, 1)."""
+    s = (seed * 1_000_003 + req * 7_919 + 3 * 104_729) & 0xFFFFFFFF
+    return to_bf16_bits(normal(s, pos * heads * dim, heads * dim)).reshape(heads, dim)
+
+
+def paged_cache(keys: list, values: list, page_size: int, seed: int, spare_pages: int = 0):
+    """Place each request's [L_b, Hkv, D] keys and values into pages of `page_size` positions,
+    the physical pages of all requests shuffled by `seed` (a seeded permutation, as a paged
+    allocator would hand them out).  Returns (k_cache, v_cache [P, page_size, Hkv, D] uint16,
+    page_table int32 [B, max_pages]); unused table entries are -1, unused page slots zero."""
+    heads, dim = keys[0].shape[1], keys[0].shape[2]
+    need = [(k.shape[0] + page_size - 1) // page_size for k in keys]
+    total = sum(need) + spare_pages
+    max_pages = max(need) if need else 0
+    perm = np.argsort(splitmix64(seed, np.arange(total, dtype=np.uint64)), kind="stable")
+    kc = np.zeros((total, page_size, heads, dim), np.uint16)
+    vc = np.zeros_like(kc)
+    table = np.full((len(keys), max(1, max_pages)), -1, np.int32)
+    nxt = 0
+    for b, (k, v) in enumerate(zip(keys, values)):
+        for pg in range(need[b]):
+            phys = int(perm[nxt])
+            nxt += 1
+            table[b, pg] = phys
+            rows = slice(pg * page_size, min((pg + 1) * page_size, k.shape[0]))
+            n = rows.stop - rows.start
+            kc[phys, :n] = k[rows]
+            vc[phys, :n] = v[rows]
+    return kc, vc, table

@@ -13,6 +13,10 @@ article; the row-wise definition y[i] = f(x[i], W) of the batch-invariance issue
 with a single round-to-nearest-even to the output dtype, and the absolute sum
 S_abs[i, j] = sum_k |dec(x[i, k]) * dec(w[k, j])| returned for the tolerance.
 
+Attention ("Batch-invariant attention", nondeterminism article): for each query token at
+position p and head, the fp64 softmax-weighted mean of the values at positions 0..p, rounded
+once to bf16, with the unrounded value and the error scales returned for the tolerance.
+
 RMSNorm ("Batch-invariant RMSNorm", nondeterminism article): for each row,
 v[i, j] = (x[i, j] / sqrt(sum_{j ascending} x[i, j]^2 / d + eps)) * g[j] in fp64,
 rounded once to bf16; v is returned for the tolerance.
@@ -62,6 +66,9 @@ def lib() -> ctypes.CDLL:
         L.bio_gemm_mxfp8.restype = ctypes.c_int
         L.bio_rmsnorm_bf16.argtypes = [P, I64, I64, P, ctypes.c_double, P, I64, P, P]
         L.bio_rmsnorm_bf16.restype = ctypes.c_int
+        L.bio_attention_bf16.argtypes = [P, I64, I64, I64, P, P, P, P, I64, I64, I64, P, I64, I64,
+                                         ctypes.c_double, P, P, P, P]
+        L.bio_attention_bf16.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -164,6 +171,35 @@ def rmsnorm_bf16(x: np.ndarray, g: np.ndarray, eps: float, rows=None):
     return y, v
 
 
+def attention_bf16(q, q_seq, q_pos, k_cache, v_cache, page_table, scale):
+    """Causal attention over a paged KV cache ("Batch-invariant attention", nondeterminism
+    article).  q uint16[T, Hq, D]; q_seq, q_pos int32[T]; k_cache, v_cache uint16[P, page, Hkv, D];
+    page_table int32[B, max_pages]; scale the fp32 value the GPU uses, passed as a double.
+
+    Returns (o uint16 [T, Hq, D], v fp64 [T, Hq, D], a fp64 [T, Hq, D], e fp64 [T, Hq]).
+    """
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint16)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint16)
+    q_seq = np.ascontiguousarray(q_seq, dtype=np.int32)
+    q_pos = np.ascontiguousarray(q_pos, dtype=np.int32)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    T, Hq, D = q.shape
+    P_, page, Hkv, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape and q_seq.shape == (T,) and q_pos.shape == (T,)
+    B, max_pages = page_table.shape
+    o = np.empty((T, Hq, D), np.uint16)
+    v = np.empty((T, Hq, D), np.float64)
+    a = np.empty((T, Hq, D), np.float64)
+    e = np.empty((T, Hq), np.float64)
+    rc = lib().bio_attention_bf16(_ptr(q), T, Hq, D, _ptr(q_seq), _ptr(q_pos), _ptr(k_cache), _ptr(v_cache),
+                                  P_, page, Hkv, _ptr(page_table), B, max_pages, float(scale),
+                                  _ptr(o), _ptr(v), _ptr(a), _ptr(e))
+    if rc:
+        raise ValueError("bio_attention_bf16 rejected its arguments")
+    return o, v, a, e
+
+
 def bf16_to_f64(b) -> float:
     return lib().bio_bf16_to_f64(int(b))
 
@@ -213,8 +249,27 @@ def tolerance_violations(y_gpu_f64: np.ndarray, y_ref_f64: np.ndarray, sabs: np.
 TOL_RMSNORM_REL = 2.0**-8 + 2.0**-16
 
 
+def attention_tolerance(v: np.ndarray, a: np.ndarray, e: np.ndarray, D: int, L: np.ndarray) -> np.ndarray:
+    """Per-element bound on |o - v| for an fp32 evaluation of the attention rounded to bf16:
+
+        2^-8 |v|  +  (4 (D + 8) u e + 2 (L + 32) u) a,      u = 2^-24
+
+    2^-8 |v| is the bf16 rounding of the output.  The second term covers fp32 arithmetic before
+    it: a score is a D-term fp32 dot product times the scale, so its absolute error is at most
+    about (D + 4) u e (e = max_j scale sum_i |q_i k_ji|); an error d in the exponent of a weight
+    changes the weight by a factor e^d, and the weights enter both the weighted sum and its
+    normaliser (hence 2 x 2 (D + 8) u e, which also absorbs the maximum's subtraction, exp's few
+    ulp and the rescaling of split partials); the two sums over L = p + 1 positions of positive
+    weights (times |v| in the numerator) add at most (L + 32) u a each in any fixed order.
+    a = sum_j w_j |v_j| / sum_j w_j bounds |v| and is the natural scale of these errors.
+    v, a [T, Hq, D]; e [T, Hq]; L [T] (key count of each query token)."""
+    u = 2.0**-24
+    L = np.asarray(L, dtype=np.float64)[:, None, None]
+    return 2.0**-8 * np.abs(v) + (4.0 * (D + 8) * u * e[:, :, None] + 2.0 * (L + 32) * u) * a
+
+
 __all__ = [
-    "rmsnorm_bf16", "TOL_RMSNORM_REL",
+    "attention_tolerance", "attention_bf16", "rmsnorm_bf16", "TOL_RMSNORM_REL",
     "gemm_f64", "gemm_bf16", "gemm_mxfp8", "bf16_to_f64", "e4m3_to_f64", "e8m0_to_f64",
     "f64_to_bf16", "f64_to_f32_bits", "bf16_array_to_f64", "TOL_BF16", "TOL_F32",
     "tolerance_violations", "lib",

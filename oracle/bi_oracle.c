@@ -1,5 +1,6 @@
 /*
- * bi_oracle.c — plain CPU oracle for the batch-invariant GEMM and RMSNorm (TEST INFRASTRUCTURE).
+ * bi_oracle.c — plain CPU oracle for the batch-invariant GEMM, RMSNorm and attention (TEST
+ * INFRASTRUCTURE).
  *
  * Only tests, the smoke check and the benchmark's CPU-baseline leg use this file.
  * It follows the plain definition C_ij = sum_k A_ik B_kj of the nondeterminism
@@ -231,5 +232,87 @@ int bio_rmsnorm_bf16(const uint16_t* x, int64_t M, int64_t d, const uint16_t* g,
             if (v) v[r * d + j] = val;
         }
     }
+    return 0;
+}
+
+/* -------------------------------------------------------------- attention */
+
+/* Straight from the definition ("Batch-invariant attention", nondeterminism article): for each
+ * query token and head, the scores of the keys at positions 0..p, their maximum, the weights
+ * exp(s - max), and the weighted mean of the values, all in fp64, rounded once to bf16. */
+int bio_attention_bf16(const uint16_t* q, int64_t T, int64_t Hq, int64_t D,
+                       const int32_t* q_seq, const int32_t* q_pos,
+                       const uint16_t* k_cache, const uint16_t* v_cache, int64_t num_pages,
+                       int64_t page_size, int64_t Hkv, const int32_t* page_table, int64_t B,
+                       int64_t max_pages, double scale, uint16_t* o, double* v, double* a, double* e) {
+    if (T < 0 || Hq <= 0 || D <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_pages < 0 || page_size <= 0 ||
+        B < 0 || max_pages < 0)
+        return -1;
+    if (T == 0) return 0;
+    if (!q || !q_seq || !q_pos || !k_cache || !v_cache || !page_table || !o) return -1;
+    const int64_t G = Hq / Hkv;
+    /* validate every position and page first */
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t b = q_seq[t], p = q_pos[t];
+        if (b < 0 || b >= B || p < 0 || p / page_size >= max_pages) return -1;
+        for (int64_t pg = 0; pg <= p / page_size; ++pg) {
+            const int64_t page = page_table[b * max_pages + pg];
+            if (page < 0 || page >= num_pages) return -1;
+        }
+    }
+    double* w = NULL;
+    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+    double* aab = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!acc || !aab) { free(acc); free(aab); return -1; }
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t b = q_seq[t], p = q_pos[t];
+        double* ww = (double*)realloc(w, sizeof(double) * (size_t)(p + 1));
+        if (!ww) { free(w); free(acc); free(aab); return -1; }
+        w = ww;
+        for (int64_t h = 0; h < Hq; ++h) {
+            const int64_t kh = h / G;
+            const uint16_t* qv = q + (t * Hq + h) * D;
+            double m = -INFINITY, emax = 0.0;
+            for (int64_t j = 0; j <= p; ++j) {
+                const int64_t page = page_table[b * max_pages + j / page_size];
+                const uint16_t* kr = k_cache + ((page * page_size + j % page_size) * Hkv + kh) * D;
+                double sdot = 0.0, sabs = 0.0;
+                for (int64_t i = 0; i < D; ++i) {
+                    const double prod = bio_bf16_to_f64(qv[i]) * bio_bf16_to_f64(kr[i]);
+                    sdot = sdot + prod;
+                    sabs = sabs + fabs(prod);
+                }
+                w[j] = scale * sdot;
+                if (w[j] > m) m = w[j];
+                if (scale * sabs > emax) emax = scale * sabs;
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j <= p; ++j) {
+                w[j] = exp(w[j] - m);
+                l = l + w[j];
+            }
+            for (int64_t i = 0; i < D; ++i) { acc[i] = 0.0; aab[i] = 0.0; }
+            for (int64_t j = 0; j <= p; ++j) {
+                const int64_t page = page_table[b * max_pages + j / page_size];
+                const uint16_t* vr = v_cache + ((page * page_size + j % page_size) * Hkv + kh) * D;
+                for (int64_t i = 0; i < D; ++i) {
+                    const double vv = bio_bf16_to_f64(vr[i]);
+                    acc[i] = acc[i] + w[j] * vv;
+                    aab[i] = aab[i] + w[j] * fabs(vv);
+                }
+            }
+            const int64_t base = (t * Hq + h) * D;
+            for (int64_t i = 0; i < D; ++i) {
+                const double val = acc[i] / l;
+                o[base + i] = bio_f64_to_bf16(val);
+                if (v) v[base + i] = val;
+                if (a) a[base + i] = aab[i] / l;
+            }
+            if (e) e[t * Hq + h] = emax;
+        }
+    }
+    free(w);
+    free(acc);
+    free(aab);
     return 0;
 }

@@ -1,6 +1,6 @@
 /*
  * bi_oracle.h — plain, slow CPU oracle for the batch-invariant GEMM y = x·W
- * (and the batch-invariant RMSNorm, declared at the end).
+ * (and the batch-invariant RMSNorm and decode attention, declared at the end).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
  * CPU-baseline leg may load this library.  The product path (the CUDA library and
@@ -80,6 +80,28 @@ int bio_gemm_mxfp8(const uint8_t* x, const uint8_t* sx, int64_t M, int64_t K,
  * M > 0, NaN or negative eps). */
 int bio_rmsnorm_bf16(const uint16_t* x, int64_t M, int64_t d, const uint16_t* g, double eps,
                      const int64_t* rows, int64_t nrows, uint16_t* y, double* v);
+
+/* Causal attention of query tokens over a paged bf16 KV cache ("Batch-invariant attention",
+ * nondeterminism article: O_i = sum_{j <= i} softmax(q_i . k_j / sqrt(d)) v_j, with the K/V
+ * cache filled before the attention runs).  For query token t (request b = q_seq[t], position
+ * p = q_pos[t]) and query head h (KV head h / G, G = Hq / Hkv):
+ *
+ *     s_j   = scale * sum_{i ascending} q[t,h,i] * K_b[j, h/G, i]          j = 0..p  (fp64)
+ *     m     = max_j s_j,   w_j = exp(s_j - m)
+ *     v[i]  = (sum_{j ascending} w_j * V_b[j, h/G, i]) / (sum_{j ascending} w_j)
+ *     o     = RNE bf16 of v
+ *
+ * K_b[j, kh, i] = k_cache[page_table[b * max_pages + j / page_size], j % page_size, kh, i]
+ * (V alike); k_cache and v_cache are [num_pages, page_size, Hkv, D] bf16 patterns, q and o
+ * [T, Hq, D].  Optional fp64 outputs, [T, Hq, D] unless noted: v (unrounded), a = (sum_j w_j
+ * |V_b[j, h/G, i]|) / (sum_j w_j) and, per [T, Hq], e = max_j scale * sum_i |q_i K_b[j, i]|
+ * (the scale of the score rounding errors) — both for the tolerance.  Returns -1 on a bad
+ * argument (sizes, Hq % Hkv, a position or page index out of range). */
+int bio_attention_bf16(const uint16_t* q, int64_t T, int64_t Hq, int64_t D,
+                       const int32_t* q_seq, const int32_t* q_pos,
+                       const uint16_t* k_cache, const uint16_t* v_cache, int64_t num_pages,
+                       int64_t page_size, int64_t Hkv, const int32_t* page_table, int64_t B,
+                       int64_t max_pages, double scale, uint16_t* o, double* v, double* a, double* e);
 
 #ifdef __cplusplus
 }
