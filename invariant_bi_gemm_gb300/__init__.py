@@ -41,6 +41,9 @@ EXPORTED_SYMBOLS = (
 )
 # every symbol include/bi_rmsnorm.h declares
 RMSNORM_EXPORTED_SYMBOLS = ("bi_rmsnorm_create", "bi_rmsnorm_run", "bi_rmsnorm_get_config", "bi_rmsnorm_destroy")
+# every symbol include/bi_attention.h declares
+ATTENTION_EXPORTED_SYMBOLS = ("bi_attention_create", "bi_attention_run", "bi_attention_workspace_size",
+                              "bi_attention_get_device_error", "bi_attention_get_config", "bi_attention_destroy")
 
 
 class BiGemmError(RuntimeError):
@@ -67,6 +70,11 @@ class bi_rmsnorm_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("d", "threads", "vectors_per_thread", "max_ctas", "num_sms")]
 
 
+class bi_attention_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_q_heads", "num_kv_heads", "head_dim", "page_size", "split_size",
+                                              "threads", "stage_positions", "max_ctas", "num_sms")]
+
+
 def _load() -> ctypes.CDLL:
     path = _build.lib_path("libbi_gemm.so")
     if not os.path.exists(path):
@@ -90,8 +98,15 @@ def _load() -> ctypes.CDLL:
     L.bi_rmsnorm_run.argtypes = [P, P, I64, P, P, P]
     L.bi_rmsnorm_get_config.argtypes = [P, ctypes.POINTER(bi_rmsnorm_config)]
     L.bi_rmsnorm_destroy.argtypes = [P]
+    L.bi_attention_create.argtypes = [ctypes.POINTER(P), I64, I64, I64, I64, ctypes.c_float, I64]
+    L.bi_attention_run.argtypes = [P, P, I64, P, P, P, P, I64, P, I64, I64, I64, P, P]
+    L.bi_attention_workspace_size.argtypes = [P, I64, I64, ctypes.POINTER(ctypes.c_uint64)]
+    L.bi_attention_get_device_error.argtypes = [P, P]
+    L.bi_attention_get_config.argtypes = [P, ctypes.POINTER(bi_attention_config)]
+    L.bi_attention_destroy.argtypes = [P]
     for n in ("bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_run_noalloc", "bi_gemm_get_device_error",
-              "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_version") + RMSNORM_EXPORTED_SYMBOLS:
+              "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_version") + \
+            RMSNORM_EXPORTED_SYMBOLS + ATTENTION_EXPORTED_SYMBOLS:
         getattr(L, n).restype = I32
     return L
 
@@ -197,6 +212,45 @@ def bi_rmsnorm_get_config(h: int) -> dict:
 
 def bi_rmsnorm_destroy(h: int) -> None:
     _check(library().bi_rmsnorm_destroy(ctypes.c_void_p(h)), "bi_rmsnorm_destroy")
+
+
+def bi_attention_create(num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int, scale: float,
+                        split_size: int = 0) -> int:
+    """Returns the handle (an opaque integer); raises BiGemmError on refusal."""
+    h = ctypes.c_void_p()
+    _check(library().bi_attention_create(ctypes.byref(h), int(num_q_heads), int(num_kv_heads), int(head_dim),
+                                         int(page_size), float(scale), int(split_size)), "bi_attention_create")
+    return h.value
+
+
+def bi_attention_run(h: int, q: int, T: int, q_seq: int, q_pos: int, k_cache: int, v_cache: int, num_pages: int,
+                     page_table: int, num_seqs: int, max_pages: int, max_pos: int, o: int, stream: int) -> None:
+    """Raw-pointer call (device addresses, stream a cudaStream_t value)."""
+    V = ctypes.c_void_p
+    rc = library().bi_attention_run(V(h), V(q), int(T), V(q_seq), V(q_pos), V(k_cache), V(v_cache), int(num_pages),
+                                     V(page_table), int(num_seqs), int(max_pages), int(max_pos), V(o), V(stream))
+    _check(rc, "bi_attention_run")
+
+
+def bi_attention_get_config(h: int) -> dict:
+    c = bi_attention_config()
+    _check(library().bi_attention_get_config(ctypes.c_void_p(h), ctypes.byref(c)), "bi_attention_get_config")
+    return {n: getattr(c, n) for n, _ in bi_attention_config._fields_}
+
+
+def bi_attention_workspace_size(h: int, T: int, max_pos: int) -> int:
+    b = ctypes.c_uint64()
+    _check(library().bi_attention_workspace_size(ctypes.c_void_p(h), int(T), int(max_pos), ctypes.byref(b)),
+           "bi_attention_workspace_size")
+    return b.value
+
+
+def bi_attention_get_device_error(h: int, stream: int = 0) -> int:
+    return library().bi_attention_get_device_error(ctypes.c_void_p(h), ctypes.c_void_p(stream))
+
+
+def bi_attention_destroy(h: int) -> None:
+    _check(library().bi_attention_destroy(ctypes.c_void_p(h)), "bi_attention_destroy")
 
 
 # --------------------------------------------------------------------- torch wrappers
@@ -327,7 +381,77 @@ class BiRmsNorm:
             pass
 
 
+class BiAttention:
+    """Batch-invariant decode attention over a paged KV cache on torch tensors.
+
+    q [T, Hq, D] bf16; k_cache, v_cache [pages, page_size, Hkv, D] bf16; page_table int32
+    [num_seqs, max_pages]; q_seq, q_pos int32 [T] (request and position of each query token).
+    """
+
+    def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+                 scale: float | None = None, split_size: int = 0):
+        self.Hq, self.Hkv, self.D, self.page_size = int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size)
+        self.scale = float(scale) if scale is not None else float(head_dim) ** -0.5
+        self.handle = bi_attention_create(self.Hq, self.Hkv, self.D, self.page_size, self.scale, split_size)
+
+    @property
+    def config(self) -> dict:
+        return bi_attention_get_config(self.handle)
+
+    def run(self, q, q_seq, q_pos, k_cache, v_cache, page_table, max_pos: int, o=None, stream=None):
+        import torch
+        T = int(q.shape[0])
+        if q.dim() != 3 or q.shape[1] != self.Hq or q.shape[2] != self.D:
+            raise ValueError("q must be [T, num_q_heads, head_dim]")
+        if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (self.page_size, self.Hkv, self.D) or \
+                v_cache.shape != k_cache.shape:
+            raise ValueError("k_cache, v_cache must be [pages, page_size, num_kv_heads, head_dim]")
+        for name, tns in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+            if tns.dtype != torch.bfloat16 or not tns.is_cuda or not tns.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+        for name, tns in (("q_seq", q_seq), ("q_pos", q_pos), ("page_table", page_table)):
+            if tns.dtype != torch.int32 or not tns.is_cuda or not tns.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+        if tuple(q_seq.shape) != (T,) or tuple(q_pos.shape) != (T,) or page_table.dim() != 2:
+            raise ValueError("q_seq, q_pos [T]; page_table [num_seqs, max_pages]")
+        if o is None:
+            o = torch.empty_like(q)
+        if o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous():
+            raise ValueError("o must be a contiguous bf16 tensor shaped like q")
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        bi_attention_run(self.handle, q.data_ptr(), T, q_seq.data_ptr(), q_pos.data_ptr(), k_cache.data_ptr(),
+                         v_cache.data_ptr(), int(k_cache.shape[0]), page_table.data_ptr(), int(page_table.shape[0]),
+                         int(page_table.shape[1]), int(max_pos), o.data_ptr(), s)
+        return o
+
+    __call__ = run
+
+    def device_error(self, stream=None) -> int:
+        s = 0
+        if stream is not None:
+            s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        return bi_attention_get_device_error(self.handle, s)
+
+    def workspace_size(self, T: int, max_pos: int) -> int:
+        return bi_attention_workspace_size(self.handle, T, max_pos)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            bi_attention_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 __all__ = [
+    "BiAttention", "bi_attention_create", "bi_attention_run", "bi_attention_get_config", "bi_attention_workspace_size",
+    "bi_attention_get_device_error", "bi_attention_destroy", "bi_attention_config", "ATTENTION_EXPORTED_SYMBOLS",
     "BiRmsNorm", "bi_rmsnorm_create", "bi_rmsnorm_run", "bi_rmsnorm_get_config", "bi_rmsnorm_destroy",
     "bi_rmsnorm_config", "RMSNORM_EXPORTED_SYMBOLS",
     "BiGemm", "BiGemmError", "bi_gemm_create", "bi_gemm_run", "bi_gemm_run_noalloc", "bi_gemm_get_device_error",

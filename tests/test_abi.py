@@ -59,6 +59,41 @@ def test_rmsnorm_null_arguments():
     assert L.bi_rmsnorm_destroy(None) == bg.BI_GEMM_OK
 
 
+def test_attention_header_symbols_exported():
+    declared = _declared("bi_attention.h")
+    assert set(declared) == set(bg.ATTENTION_EXPORTED_SYMBOLS)
+    L = ctypes.CDLL(bgbuild.lib_path("libbi_gemm.so"))
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,page,scale,split,want", [
+    (32, 8, 128, 16, 0.0, 0, bg.BI_GEMM_ERR_INVALID_ARG),
+    (32, 8, 128, 16, float("nan"), 0, bg.BI_GEMM_ERR_INVALID_ARG),
+    (32, 8, 128, 0, 0.1, 0, bg.BI_GEMM_ERR_INVALID_ARG),
+    (32, 8, 128, 16, 0.1, -1, bg.BI_GEMM_ERR_INVALID_ARG),
+    (30, 8, 128, 16, 0.1, 0, bg.BI_GEMM_ERR_UNSUPPORTED),       # heads not a multiple
+    (32, 2, 128, 16, 0.1, 0, bg.BI_GEMM_ERR_UNSUPPORTED),       # group of 16
+    (32, 8, 96, 16, 0.1, 0, bg.BI_GEMM_ERR_UNSUPPORTED),        # head dim
+    (32, 8, 128, 16, 0.1, 200, bg.BI_GEMM_ERR_UNSUPPORTED),     # split not a multiple of 128
+    (32, 8, 128, 16, 0.1, 2048, bg.BI_GEMM_ERR_UNSUPPORTED),
+])
+def test_attention_create_refuses_before_touching_cuda(Hq, Hkv, D, page, scale, split, want):
+    h = ctypes.c_void_p()
+    assert bg.library().bi_attention_create(ctypes.byref(h), Hq, Hkv, D, page, scale, split) == want
+    assert h.value is None
+
+
+def test_attention_null_arguments():
+    L = bg.library()
+    assert L.bi_attention_create(None, 32, 8, 128, 16, 0.1, 0) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_attention_run(None, None, 1, None, None, None, None, 1, None, 1, 1, 0, None, None) == \
+        bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_attention_get_device_error(None, None) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_attention_get_config(None, None) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_attention_destroy(None) == bg.BI_GEMM_OK
+
+
 def test_controls_symbols_exported():
     declared = _declared("bi_gemm_controls.h")
     assert declared, "controls header declares nothing"
