@@ -559,7 +559,73 @@ def measure_other_paths(dev, peaks):
                                           "frac_tensor": round(flops(2048, 4096, 4096) / t / 1e12 / peaks["bf16_tflops"], 3)}
     g.close()
     out["rmsnorm"] = measure_rmsnorm(dev, peaks, bf)
+    out["attention_decode"] = measure_attention(dev, peaks)
     return out
+
+
+ATTN = {"num_q_heads": 32, "num_kv_heads": 8, "head_dim": 128, "page_size": 16, "split_size": 256}
+
+
+def attention_bytes(B, L, a=ATTN):
+    """Algorithmic HBM bytes of one decode step: every request's keys and values once, its query
+    and output."""
+    return 2 * B * L * a["num_kv_heads"] * a["head_dim"] * 2 + 2 * B * a["num_q_heads"] * a["head_dim"] * 2
+
+
+def measure_attention(dev, peaks):
+    """Batch-invariant decode attention (one query token per request at its last position) over
+    a paged bf16 cache with shuffled pages, 32 query heads on 8 KV heads of 128, 16-position pages,
+    split size 256; graph-timed.  Values are seeded normals drawn on the device (timing only)."""
+    import torch
+    from invariant_bi_gemm_gb300 import BiAttention
+
+    a = ATTN
+    attn = BiAttention(a["num_q_heads"], a["num_kv_heads"], a["head_dim"], a["page_size"], split_size=a["split_size"])
+    rows = []
+    for B, L in ((1, 32768), (8, 4096), (32, 4096), (64, 8192), (256, 2048)):
+        pages_per = (L + a["page_size"] - 1) // a["page_size"]
+        P = B * pages_per
+        g = torch.Generator(device=dev).manual_seed(1234)
+        shape = (P, a["page_size"], a["num_kv_heads"], a["head_dim"])
+        kc = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        vc = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        table = torch.randperm(P, generator=g, device=dev).to(torch.int32).view(B, pages_per).contiguous()
+        q = torch.randn((B, a["num_q_heads"], a["head_dim"]), generator=g, device=dev).to(torch.bfloat16)
+        q_seq = torch.arange(B, dtype=torch.int32, device=dev)
+        q_pos = torch.full((B,), L - 1, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        fn = lambda: attn(q, q_seq, q_pos, kc, vc, table, L - 1, o)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        reps = 10
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for _ in range(reps):
+                fn()
+        gr.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            gr.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / reps / 1e3)
+        t = statistics.median(ts)
+        by = attention_bytes(B, L)
+        rows.append({"batch": B, "context": L, "us": round(t * 1e6, 2), "gbs": round(by / t / 1e9, 1),
+                     "frac_hbm": round(by / t / 1e9 / peaks["hbm_gbs"], 3)})
+        del kc, vc, table, q, o, gr
+    err = attn.device_error()
+    cfg = attn.config
+    attn.close()
+    return {"shape": "decode: q[B,32,128] over a paged bf16 KV cache [pages,16,8,128], one token per request at "
+                     "position context-1, split size 256 positions",
+            "grid_bound": cfg["max_ctas"], "rows": rows, "device_error": err,
+            "bytes": "K and V of every request once (2 x B x context x 8 x 128 x 2) + q and o",
+            "note": "graph-timed; pages shuffled over the cache; three kernels per call (plan, attention, merge)"}
 
 
 RMS_D = 4096

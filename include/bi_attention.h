@@ -19,8 +19,11 @@
  * in ascending s.  Nothing depends on the number of query tokens, on the other requests, on the
  * request's index b, on where its pages sit, or on whether its earlier tokens were processed in
  * the same call (chunked prefill): o[t] is a function of q[t], p and K_b, V_b[0..p] only, bit for
- * bit.  Arithmetic: fp32 (scores as fp32 dot products times scale * log2(e), weights exp2 of the
- * score minus the split's maximum, sums in ascending position), one bf16 rounding at the end.
+ * bit.  Arithmetic: scores on the tensor cores (bf16 products, fp32 accumulation, one fixed
+ * instruction shape) times scale * log2(e); weights exp2 of the score minus the split's maximum
+ * in fp32; the weighted sum of the values on the tensor cores with each weight split into two
+ * bf16 parts (16 significant bits) and fp32 accumulation in ascending position; fp32 merge and
+ * division; one bf16 rounding at the end.
  *
  * Conventions (as in bi_gemm.h, whose BI_GEMM_* return codes these functions use):
  *   - q [T, num_q_heads, head_dim] and o likewise, bf16 row-major; k_cache, v_cache
@@ -68,8 +71,9 @@ int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, int64_t num_kv
 /* o = attention(q) for T query tokens.  max_pos: an upper bound (on the host) of every q_pos;
  * it sizes the workspace and the grid and changes no result.  T = 0 queues nothing.  The run
  * grows the handle's workspace (stream-ordered cudaMallocAsync) when T or max_pos outgrow it
- * (BI_GEMM_ERR_OOM if that fails), then queues two kernels on `stream`: a plan of the
- * (token, KV head, split) units and the attention itself.  Asynchronous. */
+ * (BI_GEMM_ERR_OOM if that fails), then queues three kernels on `stream`: a plan of the
+ * (token, KV head, split) units, the attention of every unit, and the merge of the splits of
+ * tokens that have more than one.  Asynchronous. */
 int bi_attention_run(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,
                      const int32_t* q_pos, const void* k_cache, const void* v_cache,
                      int64_t num_pages, const int32_t* page_table, int64_t num_seqs,

@@ -4,24 +4,28 @@
 // "Batch-invariant attention" (nondeterminism article): split the keys of a query at a fixed
 // split SIZE, reduce each split in one fixed order, merge the splits in a fixed order.  The
 // work unit is (query token t, KV head kh, split s); one block of 128 threads runs a unit:
-//   1. the G query heads of kh are widened to fp32 in shared memory;
-//   2. the split's keys, then its values, stream through a 3-deep ring of 128-position stages
-//      (cp.async, 16-byte chunks, row-XOR swizzle so that both passes read without bank
-//      conflicts); rows past p, or of an invalid page, are zero-filled and masked;
-//   3. pass 1: thread r owns position r of a key stage and computes its G scores as fp32 dot
-//      products in ascending dimension (fmaf), times scale * log2(e);
-//   4. per head, the split's maximum m (exact, order-free) and weights w_j = exp2(s_j - m);
-//   5. pass 2: each thread owns G*D/128 consecutive outputs of one head and accumulates
-//      acc += w_j v_j and l += w_j over the split's positions in ascending order;
-//   6. a single-split token writes bf16(acc / l); otherwise the unit stores (m, l, acc) and the
-//      last of the token's split blocks to arrive (an integer counter) merges all splits in
-//      ascending s: M = max m_s, L = sum l_s 2^(m_s - M), A = sum acc_s 2^(m_s - M), o = A / L.
-//      A single split merged this way gives the same bits as the direct path (2^0 = 1).
+//   1. the G query heads of kh are held in registers as MMA A fragments;
+//   2. the split's keys, then its values, stream through a 2-deep ring of 64-position stages
+//      (cp.async, 16-byte chunks, row-XOR swizzle so that the ldmatrix reads of both passes are
+//      free of bank conflicts); rows past p, or of an invalid page, are zero-filled and masked;
+//   3. pass 1: the G x 128 scores of a key stage, Q K^T on the tensor cores (mma.sync m16n8k16,
+//      bf16 in, fp32 accumulate; the G heads are rows 0..G-1 of the 16-row instruction, each
+//      warp 32 positions, k in ascending order), times scale * log2(e);
+//   4. per head, the split's maximum m (exact, order-free), the weights w_j = exp2(s_j - m) and
+//      their sum l (each thread its positions in order, then a fixed butterfly and warp order);
+//   5. pass 2: O += P V on the tensor cores, 16 positions per step in ascending order, each warp
+//      a quarter of the dimensions; the fp32 weights enter as two bf16 parts (hi = bf16(w),
+//      lo = bf16(w - hi), two MMAs), so the products carry 16 of the weights' bits, not 8;
+//   6. a single-split token writes bf16(acc / l); otherwise the unit stores (m, l, acc), and a
+//      merge kernel combines the splits of each (token, KV head) in ascending s:
+//      M = max m_s, L = sum l_s 2^(m_s - M), A = sum acc_s 2^(m_s - M), o = A / L.
+//      A single split merged this way would give the same bits as the direct path (2^0 = 1).
 // A plan kernel first turns q_pos into per-token unit offsets (a prefix sum) and the token of
-// every unit, and zeroes the counters.  The attention kernel is persistent: a block fetches its
-// next unit's coordinates, page indices and query while it works on the current one and issues
-// the next unit's first stages into the ring during the current unit's last ones, so that the
-// key/value stream does not drain between units.
+// every unit.  The attention kernel is persistent: a block fetches its next unit's coordinates,
+// row offsets and query while it works on the current one and issues the next unit's first
+// stages into the ring during the current unit's last ones, so that the key/value stream does
+// not drain between units; with the merge in a kernel of its own a unit ends without any fence
+// or counter.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -41,8 +45,9 @@ namespace biattn {
 
 namespace ptx = bigemm::ptx;
 
-constexpr int kThreads = 128;        // threads per block = positions per stage
-constexpr int kStages = 3;           // staging ring depth
+constexpr int kThreads = 128;        // threads per block (four warps)
+constexpr int kStagePos = 64;        // positions per staged key / value tile
+constexpr int kStages = 2;           // staging ring depth (more blocks per SM beat a deeper ring)
 constexpr int kDefaultSplit = 256;
 constexpr uint32_t kErrInput = 1u;   // bad q_seq / q_pos / page-table extent
 constexpr uint32_t kErrPage = 2u;    // page index outside [0, num_pages)
@@ -58,13 +63,11 @@ struct Params {
   uint16_t* o;
   int32_t* cum;      // [T + 1] first unit of each token
   int32_t* umap;     // [units] the token of each unit
-  uint32_t* cnt;     // [T * Hkv] merge counters
   float* part;       // [T * Hkv * max_splits, G, D] partial weighted sums
   float* ml;         // [T * Hkv * max_splits, G, 2] (maximum, sum of weights)
   uint32_t* status;
   int64_t T, num_pages, B, max_pages;
   int32_t Hq, Hkv, page_size, split, max_splits;
-  int32_t pages_per_split;   // most pages one split can touch
   float c;           // scale * log2(e)
 };
 
@@ -72,18 +75,12 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_f(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
-__device__ __forceinline__ uint16_t f_bf16(float f) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(0.0f), "f"(f));
-  return uint16_t(r & 0xFFFFu);
-}
 
 // Number of splits of a token at position p.
 __device__ __forceinline__ int32_t splits_of(int32_t p, int32_t split) { return p / split + 1; }
 
 // Unit offsets: cum[t] = Hkv * (splits of the tokens before t) and the token of every unit; a
-// token with an input the kernel cannot serve gets no units (and sets the status word).  Also
-// zeroes the merge counters.
+// token with an input the kernel cannot serve gets no units (and sets the status word).
 __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
@@ -102,7 +99,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
       } else {
         n = splits_of(pos, p.split) * p.Hkv;
       }
-      for (int kh = 0; kh < p.Hkv; ++kh) p.cnt[t * p.Hkv + kh] = 0u;
     }
     int32_t x = n;   // inclusive scan within the warp, then over the warps
 #pragma unroll
@@ -138,39 +134,57 @@ template <int D, int G>
 struct Cfg {
   static constexpr int CHUNKS = D / 8;                 // 16-byte chunks per row
   static constexpr int ROW_BYTES = D * 2;
-  static constexpr int STAGE_BYTES = kThreads * ROW_BYTES;
-  static constexpr int OPT = (G * D) / kThreads >= 1 ? (G * D) / kThreads : 1;   // outputs per thread
-  static constexpr int OUT_THREADS = G * D / OPT;
-  static_assert(OPT == 1 || OPT == 2 || OPT == 4 || OPT == 8, "outputs per thread");
-  static_assert(OUT_THREADS <= kThreads, "output threads");
-  static size_t smem_bytes(int split, int pages_per_split) {
-    return size_t(kStages) * STAGE_BYTES + sizeof(float) * (size_t(G) * D + size_t(G) * split + G * 4) +
-           sizeof(int32_t) * 2 * size_t(pages_per_split);
+  static constexpr int STAGE_BYTES = kStagePos * ROW_BYTES;
+  static constexpr int CHUNKS_PER_THREAD = kStagePos * CHUNKS / kThreads;
+  static constexpr int NT1 = kStagePos / 4 / 8;        // score n tiles (8 positions) per warp
+  static constexpr int QS = D + 8;                     // query row stride in shared memory
+  static constexpr int KSTEPS = D / 16;                // k steps of the score MMA
+  static constexpr int DW = D / 4;                     // output dimensions per warp
+  static constexpr int NT2 = DW / 8;                   // n tiles per warp in the value MMA
+  static_assert(G <= 8, "the query heads of a group fill at most 8 of the MMA's 16 rows");
+  static_assert(NT2 % 2 == 0, "n tiles are loaded in pairs");
+  // score row stride (floats): a multiple of 8 keeps float2 rows aligned; +8 spreads the banks
+  __host__ __device__ static int sc_stride(int split) { return split + 8; }
+  // ring | row offsets [2][split] (int64) | scores [G][stride] | per-warp maxima [G][4] |
+  // per-warp sums [G][4] | maximum [G] | sum [G] | query rows [2][G][QS] (bf16)
+  static size_t smem_bytes(int split) {
+    return size_t(kStages) * STAGE_BYTES + sizeof(int64_t) * 2 * size_t(split) +
+           sizeof(float) * (size_t(G) * sc_stride(split) + G * 10) + sizeof(uint16_t) * 2 * G * QS;
   }
 };
 
-// Load OPT consecutive bf16 (at dimension d, a multiple of OPT) of a staged row as fp32.
-template <int OPT>
-__device__ __forceinline__ void load_piece(const uint8_t* p, float (&v)[OPT]) {
-  if constexpr (OPT == 8) {
-    const uint4 w = *reinterpret_cast<const uint4*>(p);
-    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-  } else if constexpr (OPT == 4) {
-    const uint2 w = *reinterpret_cast<const uint2*>(p);
-    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-  } else if constexpr (OPT == 2) {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-    v[0] = bf16_lo(w); v[1] = bf16_hi(w);
-  } else {
-    v[0] = bf16_f(*reinterpret_cast<const uint16_t*>(p));
-  }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// d += a * b on the tensor cores: a 16 x 16 (row-major, bf16), b 16 x 8 (column-major, bf16),
+// d 16 x 8 fp32.  Rows 8..15 of a are zero here (a1 = a3 = 0): the query heads use rows 0..7.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 
 // One unit's coordinates, read from the plan.
 struct Unit {
   int64_t t, b;
-  int32_t kh, s, pos, nsplit, j0, valid, nsub, page0, npages;
+  int32_t kh, s, pos, nsplit, j0, valid, nsub;
 };
 
 __device__ __forceinline__ Unit unit_of(const Params& p, int64_t u) {
@@ -184,49 +198,48 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int64_t u) {
   w.nsplit = splits_of(w.pos, p.split);
   w.j0 = w.s * p.split;
   w.valid = min(p.split, w.pos + 1 - w.j0);                  // keys in this split (>= 1)
-  w.nsub = (w.valid + kThreads - 1) / kThreads;
-  w.page0 = w.j0 / p.page_size;
-  w.npages = (w.j0 + w.valid - 1) / p.page_size - w.page0 + 1;
+  w.nsub = (w.valid + kStagePos - 1) / kStagePos;
   return w;
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads) attn_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
   using C = Cfg<D, G>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  float* qs = reinterpret_cast<float*>(smem + kStages * C::STAGE_BYTES);   // [G][D]
-  float* sc = qs + G * D;                                                   // [G][split]
-  float* red = sc + G * p.split;                                            // [G][4]
-  int32_t* pages = reinterpret_cast<int32_t*>(red + G * 4);                 // [2][max_pages_per_split]
-  __shared__ uint32_t s_last;
+  const int SCS = C::sc_stride(p.split);
+  int64_t* rowoff = reinterpret_cast<int64_t*>(smem + kStages * C::STAGE_BYTES);   // [2][split]
+  float* sc = reinterpret_cast<float*>(rowoff + 2 * p.split);               // [G][SCS] scores, then weights
+  float* red = sc + G * SCS;                                                // [G][4] per-warp maxima
+  float* redl = red + G * 4;                                                // [G][4] per-warp sums
+  float* hm = redl + G * 4;                                                 // [G] maximum of the split
+  float* hl = hm + G;                                                       // [G] sum of its weights
+  uint16_t* qsm = reinterpret_cast<uint16_t*>(hl + G);                      // [2][G][D + 8] query rows
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
-  const int og = (tid * C::OPT) / D, od = (tid * C::OPT) % D;   // pass-2 outputs: head, first dim
-  const bool has_out = tid < C::OUT_THREADS;
-  constexpr int QPT = G * D / kThreads >= 1 ? G * D / kThreads : 1;   // query elements per thread
+  const int gq = lane >> 2, tq = lane & 3;       // MMA fragment coordinates: row (head), pair
+  const bool row_ok = gq < G;
+  const int dbase = warp * C::DW;               // this warp's output dimensions
 
   const int32_t total = p.cum[p.T];
   int64_t u = blockIdx.x;
   if (u >= total) return;
 
-  // A unit's page indices go to its half of `pages`; its query heads, widened, to qs.
-  auto fill_pages = [&](const Unit& w, int half) {
-    for (int i = tid; i < w.npages; i += kThreads)
-      pages[half * p.pages_per_split + i] = p.table[w.b * p.max_pages + w.page0 + i];
-  };
-  auto load_q = [&](const Unit& w, uint16_t (&qr)[QPT]) {
-#pragma unroll
-    for (int e = 0; e < QPT; ++e) {
-      const int i = tid * QPT + e;
-      qr[e] = i < G * D ? p.q[(w.t * p.Hq + int64_t(w.kh) * G) * D + i] : uint16_t(0);
+  // Element offset of each key / value row of a unit's split in the caches (without the KV head),
+  // or -1 for a row whose page index is outside [0, num_pages).
+  auto fill_rows = [&](const Unit& w, int half) {
+    for (int jl = tid; jl < w.valid; jl += kThreads) {
+      const int32_t j = w.j0 + jl;
+      const int64_t page = p.table[w.b * p.max_pages + j / p.page_size];
+      rowoff[half * p.split + jl] =
+          (page >= 0 && page < p.num_pages) ? (page * p.page_size + j % p.page_size) * p.Hkv * D : int64_t(-1);
     }
   };
-  auto store_q = [&](const uint16_t (&qr)[QPT]) {
-#pragma unroll
-    for (int e = 0; e < QPT; ++e) {
-      const int i = tid * QPT + e;
-      if (i < G * D) qs[i] = bf16_f(qr[e]);
-    }
+  // A unit's G query rows go to its half of qsm (rows padded by 8 elements, so that the
+  // fragment reads of the eight heads fall in different banks).
+  auto load_q = [&](const Unit& w, int half) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q + (w.t * p.Hq + int64_t(w.kh) * G) * D);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(qsm + half * G * C::QS);
+    for (int i = tid; i < G * D / 2; i += kThreads) dst[(i / (D / 2)) * (C::QS / 2) + i % (D / 2)] = src[i];
   };
 
   bool bad_page = false;
@@ -236,19 +249,20 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const Params p) {
     const int sub = isv ? i - w.nsub : i;
     const uint16_t* base = isv ? p.vc : p.kc;
     const uint32_t dst0 = ptx::smem_u32(ring + slot * C::STAGE_BYTES);
-    const int32_t* pg = pages + half * p.pages_per_split;
+    const int64_t* ro = rowoff + half * p.split + sub * kStagePos;
+    const uint16_t* hbase = base + int64_t(w.kh) * D;
+    const int rows = w.valid - sub * kStagePos;
 #pragma unroll 4
-    for (int it = 0; it < C::CHUNKS; ++it) {
+    for (int it = 0; it < C::CHUNKS_PER_THREAD; ++it) {
       const int lin = it * kThreads + tid;
       const int row = lin / C::CHUNKS, c = lin % C::CHUNKS;
       const uint32_t dst = dst0 + row * C::ROW_BYTES + ((c ^ (row & (C::CHUNKS - 1))) << 4);
       const void* src = base;
       uint32_t bytes = 0;
-      if (sub * kThreads + row < w.valid) {
-        const int32_t j = w.j0 + sub * kThreads + row;
-        const int64_t page = pg[j / p.page_size - w.page0];
-        if (page >= 0 && page < p.num_pages) {
-          src = base + ((page * p.page_size + j % p.page_size) * p.Hkv + w.kh) * D + c * 8;
+      if (row < rows) {
+        const int64_t off = ro[row];
+        if (off >= 0) {
+          src = hbase + off + c * 8;
           bytes = 16;
         } else {
           bad_page = true;
@@ -257,15 +271,15 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const Params p) {
       ptx::cp_async_16(dst, src, bytes);   // bytes == 0: zero-fill, nothing read
     }
   };
+  // Shared-memory address of 16-byte chunk c of staged row r.
+  auto chunk_addr = [&](uint32_t stage, int r, int c) {
+    return stage + r * C::ROW_BYTES + ((c ^ (r & (C::CHUNKS - 1))) << 4);
+  };
 
   Unit cur = unit_of(p, u);
   int half = 0;
-  {
-    uint16_t qr[QPT];
-    load_q(cur, qr);
-    fill_pages(cur, half);
-    store_q(qr);
-  }
+  load_q(cur, half);
+  fill_rows(cur, half);
   __syncthreads();
   uint32_t seq = 0;   // sequence number of the next load to issue (its ring slot is seq % kStages)
   uint32_t cons = 0;  // sequence number of the next load to consume
@@ -276,69 +290,72 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const Params p) {
   }
 
   while (true) {
-    // the next unit of this block: its coordinates, pages and query are fetched now, so that
-    // its first stages can be issued while this unit finishes
+    // The next unit of this block: its coordinates, row offsets and query are fetched while this
+    // unit's first stage is awaited (or up front when this unit has a single key stage, since
+    // the next unit's first load is then issued right away), so that its first stages can be
+    // issued during this unit's last ones.
     const int64_t un = u + gridDim.x;
     const bool has_next = un < total;
     Unit nxt;
-    uint16_t qn[QPT];
-    if (has_next) {
-      nxt = unit_of(p, un);
-      fill_pages(nxt, half ^ 1);
-      load_q(nxt, qn);
-    }
-    __syncthreads();   // the next unit's pages are visible to every issuing thread
-
+    auto fetch_next = [&]() {
+      if (has_next) {
+        nxt = unit_of(p, un);
+        fill_rows(nxt, half ^ 1);
+        load_q(nxt, half ^ 1);
+      }
+    };
     const int nload = 2 * cur.nsub;
-    float acc[C::OPT];
+    if (nload <= kStages - 1) {
+      fetch_next();
+      __syncthreads();   // the next unit's row offsets are visible to every issuing thread
+    }
+    float acc[C::NT2][4];
 #pragma unroll
-    for (int e = 0; e < C::OPT; ++e) acc[e] = 0.0f;
-    float l = 0.0f;
+    for (int n = 0; n < C::NT2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
     for (int i = 0; i < nload; ++i) {
       const int ahead = i + kStages - 1;   // the load issued now: this unit's, or the next's
       if (ahead < nload) issue(cur, half, ahead, int(seq % kStages));
       else if (has_next && ahead - nload < 2 * nxt.nsub) issue(nxt, half ^ 1, ahead - nload, int(seq % kStages));
       ++seq;
       ptx::cp_async_commit();
+      if (i == 0 && nload > kStages - 1) fetch_next();   // visible after the barrier below
       ptx::cp_async_wait<kStages - 1>();
       __syncthreads();
-      const uint8_t* buf = ring + (cons % kStages) * C::STAGE_BYTES;
+      const uint32_t stage = ptx::smem_u32(ring + (cons % kStages) * C::STAGE_BYTES);
       ++cons;
       if (i < cur.nsub) {
-        // pass 1: the scores of position jl for the G heads
-        const int row = tid, jl = i * kThreads + row;
-        if (jl < cur.valid) {
-          float dot[G];
+        // pass 1: scores of this warp's quarter of the stage, S = Q K^T on the tensor cores,
+        // fixed k order; row gq (a query head) of each n tile, columns 2tq and 2tq + 1
+        const int pos0 = i * kStagePos + warp * (kStagePos / 4);
+        // query A fragments: a0 = q[gq][16k + 2tq, +1], a2 = q[gq][16k + 8 + 2tq, +1]
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qsm + (half * G + (row_ok ? gq : 0)) * C::QS);
 #pragma unroll
-          for (int g = 0; g < G; ++g) dot[g] = 0.0f;
-#pragma unroll 4
-          for (int c = 0; c < C::CHUNKS; ++c) {
-            float kf[8];
-            load_piece<8>(buf + row * C::ROW_BYTES + ((c ^ (row & (C::CHUNKS - 1))) << 4), kf);
+        for (int nt = 0; nt < C::NT1; ++nt) {
+          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          const int prow = warp * (kStagePos / 4) + nt * 8 + (lane & 7);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const float4 q0 = *reinterpret_cast<const float4*>(qs + g * D + c * 8);
-              const float4 q1 = *reinterpret_cast<const float4*>(qs + g * D + c * 8 + 4);
-              dot[g] = __fmaf_rn(q0.x, kf[0], dot[g]);
-              dot[g] = __fmaf_rn(q0.y, kf[1], dot[g]);
-              dot[g] = __fmaf_rn(q0.z, kf[2], dot[g]);
-              dot[g] = __fmaf_rn(q0.w, kf[3], dot[g]);
-              dot[g] = __fmaf_rn(q1.x, kf[4], dot[g]);
-              dot[g] = __fmaf_rn(q1.y, kf[5], dot[g]);
-              dot[g] = __fmaf_rn(q1.z, kf[6], dot[g]);
-              dot[g] = __fmaf_rn(q1.w, kf[7], dot[g]);
-            }
+          for (int kp = 0; kp < C::KSTEPS / 2; ++kp) {
+            uint32_t b[4];
+            ldsm_x4(chunk_addr(stage, prow, 4 * kp + (lane >> 3)), b);
+            const int k0 = 2 * kp, k1 = 2 * kp + 1;
+            const uint32_t a00 = row_ok ? qrow[8 * k0 + tq] : 0u, a02 = row_ok ? qrow[8 * k0 + 4 + tq] : 0u;
+            const uint32_t a10 = row_ok ? qrow[8 * k1 + tq] : 0u, a12 = row_ok ? qrow[8 * k1 + 4 + tq] : 0u;
+            mma16816(d, a00, a02, b[0], b[1]);
+            mma16816(d, a10, a12, b[2], b[3]);
           }
-#pragma unroll
-          for (int g = 0; g < G; ++g) sc[g * p.split + jl] = __fmul_rn(dot[g], p.c);
+          const int jl = pos0 + nt * 8 + 2 * tq;
+          if (row_ok) {
+            if (jl < cur.valid) sc[gq * SCS + jl] = __fmul_rn(d[0], p.c);
+            if (jl + 1 < cur.valid) sc[gq * SCS + jl + 1] = __fmul_rn(d[1], p.c);
+          }
         }
         if (i == cur.nsub - 1) {
-          // the split's maximum per head, then the weights in place
+          // the split's maximum per head, the weights in place and their sum (fixed tree)
           __syncthreads();
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             float m = -INFINITY;
-            for (int jj = tid; jj < cur.valid; jj += kThreads) m = fmaxf(m, sc[g * p.split + jj]);
+            for (int jj = tid; jj < cur.valid; jj += kThreads) m = fmaxf(m, sc[g * SCS + jj]);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
             if (lane == 0) red[g * 4 + warp] = m;
@@ -347,77 +364,84 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const Params p) {
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             const float m = fmaxf(fmaxf(red[g * 4 + 0], red[g * 4 + 1]), fmaxf(red[g * 4 + 2], red[g * 4 + 3]));
-            for (int jj = tid; jj < cur.valid; jj += kThreads)
-              sc[g * p.split + jj] = exp2f(__fsub_rn(sc[g * p.split + jj], m));
-          }
-        }
-      } else if (has_out) {
-        // pass 2: weighted sum of the value rows of this stage, ascending position
-        const int sub = i - cur.nsub;
-        const int rows = min(kThreads, cur.valid - sub * kThreads);
-        const float* w = sc + og * p.split + sub * kThreads;
-        const int chunk = od / 8, within = (od % 8) * 2;
-#pragma unroll 4
-        for (int row = 0; row < rows; ++row) {
-          float v[C::OPT];
-          load_piece<C::OPT>(buf + row * C::ROW_BYTES + ((chunk ^ (row & (C::CHUNKS - 1))) << 4) + within, v);
-          const float wj = w[row];
+            float ls = 0.0f;
+            for (int jj = tid; jj < cur.valid; jj += kThreads) {
+              const float w = exp2f(__fsub_rn(sc[g * SCS + jj], m));
+              sc[g * SCS + jj] = w;
+              ls = __fadd_rn(ls, w);
+            }
 #pragma unroll
-          for (int e = 0; e < C::OPT; ++e) acc[e] = __fmaf_rn(wj, v[e], acc[e]);
-          l = __fadd_rn(l, wj);
+            for (int o = 16; o > 0; o >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xFFFFFFFFu, ls, o));
+            if (tid == 0) hm[g] = m;
+            if (lane == 0) redl[g * 4 + warp] = ls;
+          }
+          __syncthreads();
+          if (tid < G)
+            hl[tid] = __fadd_rn(__fadd_rn(__fadd_rn(redl[tid * 4 + 0], redl[tid * 4 + 1]), redl[tid * 4 + 2]),
+                                redl[tid * 4 + 3]);
+        }
+      } else {
+        // pass 2: O += P V over this stage's positions, 16 at a time, on the tensor cores;
+        // P (fp32) enters as two bf16 parts, hi = bf16(P) and lo = bf16(P - hi), each an MMA
+        const int sub = i - cur.nsub;
+        const int rows = min(kStagePos, cur.valid - sub * kStagePos);
+        for (int k0 = 0; k0 < rows; k0 += 16) {
+          float pw[4];
+          const int jb = sub * kStagePos + k0 + 2 * tq;   // position (within the split) of pw[0]
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int jl = jb + (e >> 1) * 8 + (e & 1);
+            pw[e] = (row_ok && jl < cur.valid) ? sc[gq * SCS + jl] : 0.0f;
+          }
+          uint32_t ah[2], al[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const float x0 = pw[2 * h2], x1 = pw[2 * h2 + 1];
+            ah[h2] = pack_bf16x2(x0, x1);
+            const float h0 = __uint_as_float(ah[h2] << 16), h1 = __uint_as_float(ah[h2] & 0xFFFF0000u);
+            al[h2] = pack_bf16x2(__fsub_rn(x0, h0), __fsub_rn(x1, h1));
+          }
+#pragma unroll
+          for (int np = 0; np < C::NT2 / 2; ++np) {
+            uint32_t b[4];
+            const int prow = k0 + ((lane >> 3) & 1) * 8 + (lane & 7);
+            ldsm_x4_trans(chunk_addr(stage, prow, (dbase + 16 * np) / 8 + (lane >> 4)), b);
+            mma16816(acc[2 * np], ah[0], ah[1], b[0], b[1]);
+            mma16816(acc[2 * np], al[0], al[1], b[0], b[1]);
+            mma16816(acc[2 * np + 1], ah[0], ah[1], b[2], b[3]);
+            mma16816(acc[2 * np + 1], al[0], al[1], b[2], b[3]);
+          }
         }
       }
       __syncthreads();
     }
 
-    const int64_t out0 = (cur.t * p.Hq + int64_t(cur.kh) * G + og) * D + od;
+    // this thread's outputs: head gq, dimensions dbase + 8n + 2tq and + 1 for each n tile
+    const int64_t orow = (cur.t * p.Hq + int64_t(cur.kh) * G + gq) * D;
     if (cur.nsplit == 1) {
-      if (has_out) {
+      if (row_ok) {
+        const float l = hl[gq];
 #pragma unroll
-        for (int e = 0; e < C::OPT; ++e) p.o[out0 + e] = f_bf16(__fdiv_rn(acc[e], l));
+        for (int n = 0; n < C::NT2; ++n)
+          *reinterpret_cast<uint32_t*>(p.o + orow + dbase + 8 * n + 2 * tq) =
+              pack_bf16x2(__fdiv_rn(acc[n][0], l), __fdiv_rn(acc[n][1], l));
       }
     } else {
       const int64_t slot0 = (cur.t * p.Hkv + cur.kh) * int64_t(p.max_splits);
       const int64_t slot = slot0 + cur.s;
-      if (has_out) {
+      if (row_ok) {
 #pragma unroll
-        for (int e = 0; e < C::OPT; ++e) p.part[(slot * G + og) * D + od + e] = acc[e];
-        if (od == 0) {
-          p.ml[(slot * G + og) * 2 + 0] =
-              fmaxf(fmaxf(red[og * 4 + 0], red[og * 4 + 1]), fmaxf(red[og * 4 + 2], red[og * 4 + 3]));
-          p.ml[(slot * G + og) * 2 + 1] = l;
-        }
+        for (int n = 0; n < C::NT2; ++n)
+          *reinterpret_cast<float2*>(p.part + (slot * G + gq) * D + dbase + 8 * n + 2 * tq) =
+              make_float2(acc[n][0], acc[n][1]);
       }
-      // Hand-off: the block's stores are ordered before the count by the barrier and the
-      // counting thread's GPU-scope fence; the block that counts last merges.
-      __syncthreads();
-      if (tid == 0) {
-        __threadfence();
-        const uint32_t old = atomicAdd(p.cnt + cur.t * p.Hkv + cur.kh, 1u);
-        s_last = old == uint32_t(cur.nsplit - 1) ? 1u : 0u;
-        if (s_last) __threadfence();
-      }
-      __syncthreads();
-      if (s_last && has_out) {
-        float M = -INFINITY;
-        for (int ss = 0; ss < cur.nsplit; ++ss) M = fmaxf(M, __ldcg(p.ml + ((slot0 + ss) * G + og) * 2));
-        float L = 0.0f, A[C::OPT];
-#pragma unroll
-        for (int e = 0; e < C::OPT; ++e) A[e] = 0.0f;
-        for (int ss = 0; ss < cur.nsplit; ++ss) {
-          const float f = exp2f(__fsub_rn(__ldcg(p.ml + ((slot0 + ss) * G + og) * 2), M));
-          L = __fadd_rn(L, __fmul_rn(__ldcg(p.ml + ((slot0 + ss) * G + og) * 2 + 1), f));
-#pragma unroll
-          for (int e = 0; e < C::OPT; ++e)
-            A[e] = __fadd_rn(A[e], __fmul_rn(__ldcg(p.part + ((slot0 + ss) * G + og) * D + od + e), f));
-        }
-#pragma unroll
-        for (int e = 0; e < C::OPT; ++e) p.o[out0 + e] = f_bf16(__fdiv_rn(A[e], L));
+      if (tid < G) {
+        p.ml[(slot * G + tid) * 2 + 0] = hm[tid];
+        p.ml[(slot * G + tid) * 2 + 1] = hl[tid];
       }
     }
     if (!has_next) break;
-    __syncthreads();   // qs and the score buffers are reused by the next unit
-    store_q(qn);
+    __syncthreads();   // scores and per-head values are reused by the next unit
     cur = nxt;
     u = un;
     half ^= 1;
@@ -425,15 +449,49 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const Params p) {
   if (bad_page) atomicOr(p.status, kErrPage);
 }
 
+// Merge of the splits of every (token, KV head) with more than one split, after all units:
+// M = max_s m_s, L = sum_s l_s 2^(m_s - M), A = sum_s acc_s 2^(m_s - M) in ascending s, o = A / L.
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads) merge_kernel(const Params p) {
+  const int64_t job = blockIdx.x;                       // token * Hkv + KV head
+  const int64_t t = job / p.Hkv;
+  const int32_t kh = int32_t(job - t * p.Hkv);
+  if (t >= p.T) return;
+  const int32_t b = p.q_seq[t], pos = p.q_pos[t];
+  if (b < 0 || b >= p.B || pos < 0 || int64_t(pos / p.page_size) >= p.max_pages) return;
+  const int32_t nsplit = splits_of(pos, p.split);
+  if (nsplit == 1 || nsplit > p.max_splits) return;    // written directly / refused by the plan
+  const int64_t slot0 = job * int64_t(p.max_splits);
+  for (int idx = int(threadIdx.x); idx < G * D / 2; idx += kThreads) {
+    const int g = idx / (D / 2), d = (idx % (D / 2)) * 2;
+    float M = -INFINITY;
+#pragma unroll 8
+    for (int ss = 0; ss < nsplit; ++ss) M = fmaxf(M, p.ml[((slot0 + ss) * G + g) * 2]);
+    float L = 0.0f, A0 = 0.0f, A1 = 0.0f;
+#pragma unroll 4
+    for (int ss = 0; ss < nsplit; ++ss) {
+      const float f = exp2f(__fsub_rn(p.ml[((slot0 + ss) * G + g) * 2], M));
+      L = __fadd_rn(L, __fmul_rn(p.ml[((slot0 + ss) * G + g) * 2 + 1], f));
+      const float2 v = *reinterpret_cast<const float2*>(p.part + ((slot0 + ss) * G + g) * D + d);
+      A0 = __fadd_rn(A0, __fmul_rn(v.x, f));
+      A1 = __fadd_rn(A1, __fmul_rn(v.y, f));
+    }
+    *reinterpret_cast<uint32_t*>(p.o + (t * p.Hq + int64_t(kh) * G + g) * D + d) =
+        pack_bf16x2(__fdiv_rn(A0, L), __fdiv_rn(A1, L));
+  }
+}
+
 struct KernelInfo {
   const void* fn = nullptr;
-  size_t (*smem)(int, int) = nullptr;
+  const void* merge = nullptr;
+  size_t (*smem)(int) = nullptr;
 };
 
 template <int D, int G>
 KernelInfo info() {
   KernelInfo k;
   k.fn = reinterpret_cast<const void*>(&attn_kernel<D, G>);
+  k.merge = reinterpret_cast<const void*>(&merge_kernel<D, G>);
   k.smem = &Cfg<D, G>::smem_bytes;
   return k;
 }
@@ -466,7 +524,6 @@ struct bi_attention {
   float scale = 0.0f;
   int device = 0, num_sms = 0, max_ctas = 0;
   size_t smem = 0;
-  int pages_per_split = 0;
   biattn::KernelInfo kern;
   uint32_t* d_status = nullptr;
   void* ws = nullptr;
@@ -476,7 +533,7 @@ struct bi_attention {
 namespace {
 
 struct WsLayout {
-  size_t cum, umap, cnt, part, ml, total;
+  size_t cum, umap, part, ml, total;
 };
 
 WsLayout layout_of(const bi_attention* h, int64_t T, int64_t max_pos) {
@@ -485,8 +542,7 @@ WsLayout layout_of(const bi_attention* h, int64_t T, int64_t max_pos) {
   WsLayout w;
   w.cum = 0;
   w.umap = biattn::align256(size_t(T + 1) * sizeof(int32_t));
-  w.cnt = w.umap + biattn::align256(size_t(slots) * sizeof(int32_t));
-  w.part = w.cnt + biattn::align256(size_t(T) * h->Hkv * sizeof(uint32_t));
+  w.part = w.umap + biattn::align256(size_t(slots) * sizeof(int32_t));
   w.ml = w.part + biattn::align256(size_t(slots) * h->G * h->D * sizeof(float));
   w.total = w.ml + biattn::align256(size_t(slots) * h->G * 2 * sizeof(float));
   return w;
@@ -518,12 +574,10 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
     return BI_GEMM_ERR_CUDA;
   }
   if (major != 10 || minor != 3) return BI_GEMM_ERR_UNSUPPORTED;
-  // the most pages one split of `split` positions can touch (its start need not be page-aligned)
-  const int pages_per_split = int(split / page_size + 2);
-  const size_t smem = k.smem(int(split), pages_per_split);
+  const size_t smem = k.smem(int(split));
   // The attribute is per kernel, shared by every handle of the same head shape: set the largest
-  // any handle of this kernel can need (split 1024, pages of one position).
-  const size_t smem_cap = k.smem(1024, 1024 + 2);
+  // any handle of this kernel can need (split 1024).
+  const size_t smem_cap = k.smem(1024);
   if (smem_cap > 232448) return BI_GEMM_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_cap)) != cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, biattn::kThreads, smem) != cudaSuccess ||
@@ -544,7 +598,6 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
   h->num_sms = sms;
   h->max_ctas = per_sm * sms;
   h->smem = smem;
-  h->pages_per_split = pages_per_split;
   h->kern = k;
   if (cudaMalloc(&h->d_status, sizeof(uint32_t)) != cudaSuccess ||
       cudaMemset(h->d_status, 0, sizeof(uint32_t)) != cudaSuccess) {
@@ -611,7 +664,6 @@ BI_GEMM_API int bi_attention_run(bi_attention_t h, const void* q, int64_t T, con
   p.o = static_cast<uint16_t*>(o);
   p.cum = reinterpret_cast<int32_t*>(ws + w.cum);
   p.umap = reinterpret_cast<int32_t*>(ws + w.umap);
-  p.cnt = reinterpret_cast<uint32_t*>(ws + w.cnt);
   p.part = reinterpret_cast<float*>(ws + w.part);
   p.ml = reinterpret_cast<float*>(ws + w.ml);
   p.status = h->d_status;
@@ -624,14 +676,15 @@ BI_GEMM_API int bi_attention_run(bi_attention_t h, const void* q, int64_t T, con
   p.page_size = h->page_size;
   p.split = h->split;
   p.max_splits = int32_t(max_pos / h->split + 1);
-  p.pages_per_split = h->pages_per_split;
   p.c = h->scale * 1.4426950408889634f;   // log2(e)
   biattn::plan_kernel<<<1, 1024, 0, st>>>(p);
   if (cudaGetLastError() != cudaSuccess) return BI_GEMM_ERR_CUDA;
   const int64_t units = T * h->Hkv * int64_t(p.max_splits);
   const unsigned grid = unsigned(std::min<int64_t>(units, h->max_ctas));
   void* args[1] = {&p};
-  if (cudaLaunchKernel(h->kern.fn, dim3(grid), dim3(biattn::kThreads), args, h->smem, st) != cudaSuccess) {
+  if (cudaLaunchKernel(h->kern.fn, dim3(grid), dim3(biattn::kThreads), args, h->smem, st) != cudaSuccess ||
+      cudaLaunchKernel(h->kern.merge, dim3(unsigned(T * h->Hkv)), dim3(biattn::kThreads), args, 0, st) !=
+          cudaSuccess) {
     cudaGetLastError();
     return BI_GEMM_ERR_CUDA;
   }
@@ -663,7 +716,7 @@ BI_GEMM_API int bi_attention_get_config(bi_attention_t h, bi_attention_config* c
   c->page_size = h->page_size;
   c->split_size = h->split;
   c->threads = biattn::kThreads;
-  c->stage_positions = biattn::kThreads;
+  c->stage_positions = biattn::kStagePos;
   c->max_ctas = h->max_ctas;
   c->num_sms = h->num_sms;
   return BI_GEMM_OK;
