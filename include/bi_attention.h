@@ -15,8 +15,10 @@
  * Batch invariance: the article's split-KV with a FIXED SPLIT SIZE (not a fixed split count):
  * the keys 0..p are cut at multiples of `split_size` positions, split s always covers
  * [s * split_size, min((s + 1) * split_size, p + 1)), every split is reduced in one fixed order
- * (the same block size, staging and thread mapping for every split), and the splits are merged
- * in ascending s.  Nothing depends on the number of query tokens, on the other requests, on the
+ * (the same block size, staging and thread mapping for every split), and the n splits are
+ * merged in one fixed order: four consecutive groups of ceil(n / 4) splits, each summed in
+ * ascending s, the group sums added in order (n is a function of p alone).  Nothing depends on
+ * the number of query tokens, on the other requests, on the
  * request's index b, on where its pages sit, or on whether its earlier tokens were processed in
  * the same call (chunked prefill): o[t] is a function of q[t], p and K_b, V_b[0..p] only, bit for
  * bit.  Arithmetic: scores on the tensor cores (bf16 products, fp32 accumulation, one fixed

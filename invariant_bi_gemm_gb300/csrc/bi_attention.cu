@@ -17,9 +17,9 @@
 //      a quarter of the dimensions; the fp32 weights enter as two bf16 parts (hi = bf16(w),
 //      lo = bf16(w - hi), two MMAs), so the products carry 16 of the weights' bits, not 8;
 //   6. a single-split token writes bf16(acc / l); otherwise the unit stores (m, l, acc), and a
-//      merge kernel combines the splits of each (token, KV head) in ascending s:
-//      M = max m_s, L = sum l_s 2^(m_s - M), A = sum acc_s 2^(m_s - M), o = A / L.
-//      A single split merged this way would give the same bits as the direct path (2^0 = 1).
+//      merge kernel combines the n splits of each (token, KV head): M = max m_s, then
+//      L = sum l_s 2^(m_s - M) and A = sum acc_s 2^(m_s - M) over four consecutive groups of
+//      splits (ascending within a group, the four group sums added in order), o = A / L.
 // A plan kernel first turns q_pos into per-token unit offsets (a prefix sum) and the token of
 // every unit.  The attention kernel is persistent: a block fetches its next unit's coordinates,
 // row offsets and query while it works on the current one and issues the next unit's first
@@ -47,6 +47,7 @@ namespace ptx = bigemm::ptx;
 
 constexpr int kThreads = 128;        // threads per block (four warps)
 constexpr int kStagePos = 64;        // positions per staged key / value tile
+constexpr int kMergeThreads = 1024;  // merge block: four threads per output pair
 constexpr int kStages = 2;           // staging ring depth (more blocks per SM beat a deeper ring)
 constexpr int kDefaultSplit = 256;
 constexpr uint32_t kErrInput = 1u;   // bad q_seq / q_pos / page-table extent
@@ -449,33 +450,69 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
   if (bad_page) atomicOr(p.status, kErrPage);
 }
 
-// Merge of the splits of every (token, KV head) with more than one split, after all units:
-// M = max_s m_s, L = sum_s l_s 2^(m_s - M), A = sum_s acc_s 2^(m_s - M) in ascending s, o = A / L.
+// Merge of the splits of every (token, KV head) with more than one split, after all units.  The
+// n splits are cut into four consecutive groups of c = ceil(n / 4); every output pair of every
+// head is handled by four threads, one per group, so that the partial loads of a long split list
+// are spread over four times the threads.  Per output, with M = max_s m_s (exact):
+//   L_q = sum_{s in group q, ascending} l_s 2^(m_s - M),  A_q = sum_{s in group q} acc_s 2^(m_s - M),
+//   L = ((L_0 + L_1) + L_2) + L_3,  A likewise,  o = A / L.
+// n depends only on the token's position, so the order is fixed for the token whatever the batch.
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads) merge_kernel(const Params p) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
+  constexpr int kPairs = G * D / 2;
+  __shared__ float sm[kPairs][4];       // group maxima, then group sums of weights
+  __shared__ float2 sa[kPairs][4];      // group weighted sums
   const int64_t job = blockIdx.x;                       // token * Hkv + KV head
   const int64_t t = job / p.Hkv;
   const int32_t kh = int32_t(job - t * p.Hkv);
   if (t >= p.T) return;
   const int32_t b = p.q_seq[t], pos = p.q_pos[t];
   if (b < 0 || b >= p.B || pos < 0 || int64_t(pos / p.page_size) >= p.max_pages) return;
-  const int32_t nsplit = splits_of(pos, p.split);
-  if (nsplit == 1 || nsplit > p.max_splits) return;    // written directly / refused by the plan
+  const int32_t n = splits_of(pos, p.split);
+  if (n == 1 || n > p.max_splits) return;    // written directly / refused by the plan
   const int64_t slot0 = job * int64_t(p.max_splits);
-  for (int idx = int(threadIdx.x); idx < G * D / 2; idx += kThreads) {
-    const int g = idx / (D / 2), d = (idx % (D / 2)) * 2;
-    float M = -INFINITY;
+  const int32_t c = (n + 3) / 4;
+  for (int it = int(threadIdx.x); it < 4 * kPairs; it += kMergeThreads) {
+    const int pr = it >> 2, q = it & 3, g = pr / (D / 2);
+    const int32_t s0 = q * c, s1 = min(n, s0 + c);
+    float m = -INFINITY;
 #pragma unroll 8
-    for (int ss = 0; ss < nsplit; ++ss) M = fmaxf(M, p.ml[((slot0 + ss) * G + g) * 2]);
+    for (int32_t ss = s0; ss < s1; ++ss) m = fmaxf(m, p.ml[((slot0 + ss) * G + g) * 2]);
+    sm[pr][q] = m;
+  }
+  __syncthreads();
+  float2 part[kPairs * 4 / kMergeThreads + 1];
+  float lpart[kPairs * 4 / kMergeThreads + 1];
+  int k = 0;
+  for (int it = int(threadIdx.x); it < 4 * kPairs; it += kMergeThreads, ++k) {
+    const int pr = it >> 2, q = it & 3, g = pr / (D / 2), d = (pr % (D / 2)) * 2;
+    const float M = fmaxf(fmaxf(sm[pr][0], sm[pr][1]), fmaxf(sm[pr][2], sm[pr][3]));
+    const int32_t s0 = q * c, s1 = min(n, s0 + c);
     float L = 0.0f, A0 = 0.0f, A1 = 0.0f;
-#pragma unroll 4
-    for (int ss = 0; ss < nsplit; ++ss) {
-      const float f = exp2f(__fsub_rn(p.ml[((slot0 + ss) * G + g) * 2], M));
-      L = __fadd_rn(L, __fmul_rn(p.ml[((slot0 + ss) * G + g) * 2 + 1], f));
+#pragma unroll 8
+    for (int32_t ss = s0; ss < s1; ++ss) {
+      const float2 ml = *reinterpret_cast<const float2*>(p.ml + ((slot0 + ss) * G + g) * 2);
+      const float f = exp2f(__fsub_rn(ml.x, M));
+      L = __fadd_rn(L, __fmul_rn(ml.y, f));
       const float2 v = *reinterpret_cast<const float2*>(p.part + ((slot0 + ss) * G + g) * D + d);
       A0 = __fadd_rn(A0, __fmul_rn(v.x, f));
       A1 = __fadd_rn(A1, __fmul_rn(v.y, f));
     }
+    part[k] = make_float2(A0, A1);
+    lpart[k] = L;
+  }
+  __syncthreads();   // every group maximum has been read
+  k = 0;
+  for (int it = int(threadIdx.x); it < 4 * kPairs; it += kMergeThreads, ++k) {
+    sm[it >> 2][it & 3] = lpart[k];
+    sa[it >> 2][it & 3] = part[k];
+  }
+  __syncthreads();
+  for (int pr = int(threadIdx.x); pr < kPairs; pr += kMergeThreads) {
+    const int g = pr / (D / 2), d = (pr % (D / 2)) * 2;
+    const float L = __fadd_rn(__fadd_rn(__fadd_rn(sm[pr][0], sm[pr][1]), sm[pr][2]), sm[pr][3]);
+    const float A0 = __fadd_rn(__fadd_rn(__fadd_rn(sa[pr][0].x, sa[pr][1].x), sa[pr][2].x), sa[pr][3].x);
+    const float A1 = __fadd_rn(__fadd_rn(__fadd_rn(sa[pr][0].y, sa[pr][1].y), sa[pr][2].y), sa[pr][3].y);
     *reinterpret_cast<uint32_t*>(p.o + (t * p.Hq + int64_t(kh) * G + g) * D + d) =
         pack_bf16x2(__fdiv_rn(A0, L), __fdiv_rn(A1, L));
   }
@@ -683,7 +720,7 @@ BI_GEMM_API int bi_attention_run(bi_attention_t h, const void* q, int64_t T, con
   const unsigned grid = unsigned(std::min<int64_t>(units, h->max_ctas));
   void* args[1] = {&p};
   if (cudaLaunchKernel(h->kern.fn, dim3(grid), dim3(biattn::kThreads), args, h->smem, st) != cudaSuccess ||
-      cudaLaunchKernel(h->kern.merge, dim3(unsigned(T * h->Hkv)), dim3(biattn::kThreads), args, 0, st) !=
+      cudaLaunchKernel(h->kern.merge, dim3(unsigned(T * h->Hkv)), dim3(biattn::kMergeThreads), args, 0, st) !=
           cudaSuccess) {
     cudaGetLastError();
     return BI_GEMM_ERR_CUDA;
