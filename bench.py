@@ -563,7 +563,7 @@ def measure_other_paths(dev, peaks):
     return out
 
 
-ATTN = {"num_q_heads": 32, "num_kv_heads": 8, "head_dim": 128, "page_size": 16, "split_size": 256}
+ATTN = {"num_q_heads": 32, "num_kv_heads": 8, "head_dim": 128, "page_size": 16, "split_size": 512}
 
 
 def attention_bytes(B, L, a=ATTN):
@@ -575,7 +575,7 @@ def attention_bytes(B, L, a=ATTN):
 def measure_attention(dev, peaks):
     """Batch-invariant decode attention (one query token per request at its last position) over
     a paged bf16 cache with shuffled pages, 32 query heads on 8 KV heads of 128, 16-position pages,
-    split size 256; graph-timed.  Values are seeded normals drawn on the device (timing only)."""
+    split size 512; graph-timed.  Values are seeded normals drawn on the device (timing only)."""
     import torch
     from invariant_bi_gemm_gb300 import BiAttention
 
@@ -622,7 +622,7 @@ def measure_attention(dev, peaks):
     cfg = attn.config
     attn.close()
     return {"shape": "decode: q[B,32,128] over a paged bf16 KV cache [pages,16,8,128], one token per request at "
-                     "position context-1, split size 256 positions",
+                     "position context-1, split size 512 positions",
             "grid_bound": cfg["max_ctas"], "rows": rows, "device_error": err,
             "bytes": "K and V of every request once (2 x B x context x 8 x 128 x 2) + q and o",
             "note": "graph-timed; pages shuffled over the cache; three kernels per call (plan, attention, merge)"}

@@ -63,7 +63,7 @@ typedef struct {
 } bi_attention_config;
 
 /* Create a handle.  Requirements (else BI_GEMM_ERR_UNSUPPORTED): head_dim 64 or 128;
- * num_q_heads / num_kv_heads = G in {1, 2, 4, 8}; page_size >= 1; split_size (0 = 256) a
+ * num_q_heads / num_kv_heads = G in {1, 2, 4, 8}; page_size >= 1; split_size (0 = 512) a
  * multiple of 128 up to 1024; an sm_103 device.  scale must be finite and > 0 (else
  * BI_GEMM_ERR_INVALID_ARG; 1 / sqrt(head_dim) is the usual value).  Checks on the arguments
  * come before any CUDA call.  *out is NULL on failure. */

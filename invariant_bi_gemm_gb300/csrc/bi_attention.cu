@@ -49,7 +49,7 @@ constexpr int kThreads = 128;        // threads per block (four warps)
 constexpr int kStagePos = 64;        // positions per staged key / value tile
 constexpr int kMergeThreads = 1024;  // merge block: four threads per output pair
 constexpr int kStages = 2;           // staging ring depth (more blocks per SM beat a deeper ring)
-constexpr int kDefaultSplit = 256;
+constexpr int kDefaultSplit = 512;
 constexpr uint32_t kErrInput = 1u;   // bad q_seq / q_pos / page-table extent
 constexpr uint32_t kErrPage = 2u;    // page index outside [0, num_pages)
 constexpr uint32_t kErrBound = 4u;   // q_pos above the host's max_pos
@@ -69,6 +69,7 @@ struct Params {
   uint32_t* status;
   int64_t T, num_pages, B, max_pages;
   int32_t Hq, Hkv, page_size, split, max_splits;
+  int32_t max_pos;   // the host's bound on q_pos
   float c;           // scale * log2(e)
 };
 
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
       const int32_t b = p.q_seq[t], pos = p.q_pos[t];
       if (b < 0 || b >= p.B || pos < 0 || int64_t(pos / p.page_size) >= p.max_pages) {
         atomicOr(p.status, kErrInput);
-      } else if (splits_of(pos, p.split) > p.max_splits) {
+      } else if (pos > p.max_pos) {
         atomicOr(p.status, kErrBound);
       } else {
         n = splits_of(pos, p.split) * p.Hkv;
@@ -469,7 +470,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
   const int32_t b = p.q_seq[t], pos = p.q_pos[t];
   if (b < 0 || b >= p.B || pos < 0 || int64_t(pos / p.page_size) >= p.max_pages) return;
   const int32_t n = splits_of(pos, p.split);
-  if (n == 1 || n > p.max_splits) return;    // written directly / refused by the plan
+  if (n == 1 || pos > p.max_pos) return;    // written directly / refused by the plan
   const int64_t slot0 = job * int64_t(p.max_splits);
   const int32_t c = (n + 3) / 4;
   for (int it = int(threadIdx.x); it < 4 * kPairs; it += kMergeThreads) {
@@ -713,6 +714,7 @@ BI_GEMM_API int bi_attention_run(bi_attention_t h, const void* q, int64_t T, con
   p.page_size = h->page_size;
   p.split = h->split;
   p.max_splits = int32_t(max_pos / h->split + 1);
+  p.max_pos = int32_t(max_pos);
   p.c = h->scale * 1.4426950408889634f;   // log2(e)
   biattn::plan_kernel<<<1, 1024, 0, st>>>(p);
   if (cudaGetLastError() != cudaSuccess) return BI_GEMM_ERR_CUDA;
