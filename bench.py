@@ -685,6 +685,45 @@ def measure_rmsnorm(dev, peaks, bf):
             "note": "graph-timed; rotating (x, y) sets > 2x L2 for every M; small M is launch-latency-bound"}
 
 
+def run_attention_only(args):
+    """Launch only the decode attention (the bench path's shape) for one batch x context, eagerly:
+    --warmup + --steps calls.  For profiling; prints the average call time as one JSON line."""
+    import torch
+    from invariant_bi_gemm_gb300 import BiAttention
+
+    dev = torch.device("cuda", 0)
+    B, L = (int(v) for v in args.attention_only.split(","))
+    a = ATTN
+    pages_per = (L + a["page_size"] - 1) // a["page_size"]
+    P = B * pages_per
+    g = torch.Generator(device=dev).manual_seed(1234)
+    shape = (P, a["page_size"], a["num_kv_heads"], a["head_dim"])
+    kc = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    vc = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    table = torch.randperm(P, generator=g, device=dev).to(torch.int32).view(B, pages_per).contiguous()
+    q = torch.randn((B, a["num_q_heads"], a["head_dim"]), generator=g, device=dev).to(torch.bfloat16)
+    q_seq = torch.arange(B, dtype=torch.int32, device=dev)
+    q_pos = torch.full((B,), L - 1, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    attn = BiAttention(a["num_q_heads"], a["num_kv_heads"], a["head_dim"], a["page_size"], split_size=a["split_size"])
+    for _ in range(args.warmup):
+        attn(q, q_seq, q_pos, kc, vc, table, L - 1, o)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        attn(q, q_seq, q_pos, kc, vc, table, L - 1, o)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / max(1, args.steps)
+    err = attn.device_error()
+    print(json.dumps({"attention_only": [B, L], "us_per_call": round(t * 1e6, 2),
+                      "gbs": round(attention_bytes(B, L) / t / 1e9, 1), "device_error": err}))
+    attn.close()
+    if err != 0:
+        sys.exit(1)
+
+
 def run_rmsnorm_only(args):
     """Launch only the RMSNorm (d = 4096) at one M, eagerly: --warmup + --steps launches.  For
     profiling; prints the average launch time as one JSON line (not the benchmark line)."""
@@ -761,6 +800,8 @@ def main():
     ap.add_argument("--no-paths", action="store_true")
     ap.add_argument("--only-m", type=int, default=0,
                     help="time a single M of the sweep only (for profiling); skips e2e, paths, CPU")
+    ap.add_argument("--attention-only", default="",
+                    help="profiling aid: 'B,L' launches only the decode attention for batch B, context L, and exits")
     ap.add_argument("--rmsnorm-only-m", type=int, default=0,
                     help="profiling aid: launch only the RMSNorm (d = 4096) at this M, eagerly, and exit")
     ap.add_argument("--mxfp8-only-m", type=int, default=0,
@@ -771,6 +812,9 @@ def main():
         return
     if args.rmsnorm_only_m:
         run_rmsnorm_only(args)
+        return
+    if args.attention_only:
+        run_attention_only(args)
         return
     if args.only_m:
         global M_SWEEP
