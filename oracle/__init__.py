@@ -17,6 +17,9 @@ Attention ("Batch-invariant attention", nondeterminism article): for each query 
 position p and head, the fp64 softmax-weighted mean of the values at positions 0..p, rounded
 once to bf16, with the unrounded value and the error scales returned for the tolerance.
 
+mHC pre-norm projection ("[BI][DSv4] Make mHC tilelang ops batch invariant"): the projection
+x_i . W divided by the root mean square of x_i, in fp64, rounded once to fp32.
+
 RMSNorm ("Batch-invariant RMSNorm", nondeterminism article): for each row,
 v[i, j] = (x[i, j] / sqrt(sum_{j ascending} x[i, j]^2 / d + eps)) * g[j] in fp64,
 rounded once to bf16; v is returned for the tolerance.
@@ -69,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.bio_attention_bf16.argtypes = [P, I64, I64, I64, P, P, P, P, I64, I64, I64, P, I64, I64,
                                          ctypes.c_double, P, P, P, P]
         L.bio_attention_bf16.restype = ctypes.c_int
+        L.bio_prenorm_gemm.argtypes = [P, I64, I64, P, I64, ctypes.c_double, P, P, P]
+        L.bio_prenorm_gemm.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -200,6 +205,36 @@ def attention_bf16(q, q_seq, q_pos, k_cache, v_cache, page_table, scale):
     return o, v, a, e
 
 
+def prenorm_gemm(x: np.ndarray, w: np.ndarray, eps: float):
+    """mHC pre-norm projection ("[BI][DSv4] Make mHC tilelang ops batch invariant"): RMSNorm of
+    each row of x (no weight) times W, in fp64, rounded once to fp32.  x uint16[M, K], w
+    uint16[K, N] (bf16 patterns); eps the fp32 value the GPU adds, passed as a double.
+
+    Returns (y float32 [M, N], v fp64 [M, N] unrounded, sabs fp64 [M, N] = sum|x w| / rms).
+    """
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    M, K = x.shape
+    K2, N = w.shape
+    assert K == K2
+    y = np.empty((M, N), np.uint32)
+    v = np.empty((M, N), np.float64)
+    sabs = np.empty((M, N), np.float64)
+    rc = lib().bio_prenorm_gemm(_ptr(x), M, K, _ptr(w), N, float(eps), _ptr(y), _ptr(v), _ptr(sabs))
+    if rc:
+        raise ValueError("bio_prenorm_gemm rejected its arguments")
+    return y.view(np.float32), v, sabs
+
+
+# mHC pre-norm projection (fp32 out): |y - v| <= TOL_PRENORM_ABS * sabs + 2^-15 |v|.  A split of K
+# into chunks of at most 512 summed in order, chunks merged in order, bounds the fp32 error of the
+# projection by gamma_{512 + S}(2^-24) sum|x w| (S <= 64 chunks for K <= 32768: 3.4e-5); the root
+# mean square adds at most 2^-16 relative (a sum of positive squares under the same bound, halved
+# by the square root, plus the division and the reciprocal square root), the product and the
+# fp32 rounding 2^-23 more.
+TOL_PRENORM_ABS = 4e-5
+
+
 def bf16_to_f64(b) -> float:
     return lib().bio_bf16_to_f64(int(b))
 
@@ -269,6 +304,7 @@ def attention_tolerance(v: np.ndarray, a: np.ndarray, e: np.ndarray, D: int, L: 
 
 
 __all__ = [
+    "prenorm_gemm", "TOL_PRENORM_ABS",
     "attention_tolerance", "attention_bf16", "rmsnorm_bf16", "TOL_RMSNORM_REL",
     "gemm_f64", "gemm_bf16", "gemm_mxfp8", "bf16_to_f64", "e4m3_to_f64", "e8m0_to_f64",
     "f64_to_bf16", "f64_to_f32_bits", "bf16_array_to_f64", "TOL_BF16", "TOL_F32",

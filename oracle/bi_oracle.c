@@ -316,3 +316,39 @@ int bio_attention_bf16(const uint16_t* q, int64_t T, int64_t Hq, int64_t D,
     free(aab);
     return 0;
 }
+
+/* ---------------------------------------------------------- mHC pre-norm GEMM */
+
+/* One row at a time, from the definition: the projection and the sum of squares in ascending k
+ * (fp64), then the projection divided by the root mean square, rounded once to fp32. */
+int bio_prenorm_gemm(const uint16_t* x, int64_t M, int64_t K, const uint16_t* w, int64_t N, double eps,
+                     uint32_t* y, double* v, double* sabs) {
+    if (M < 0 || K <= 0 || N <= 0 || !(eps >= 0.0)) return -1;
+    if (M > 0 && (!x || !w || !y)) return -1;
+    double* a = (double*)malloc(sizeof(double) * (size_t)N);
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!a || !s) { free(a); free(s); return -1; }
+    for (int64_t i = 0; i < M; ++i) {
+        double ss = 0.0;
+        for (int64_t j = 0; j < N; ++j) { a[j] = 0.0; s[j] = 0.0; }
+        for (int64_t k = 0; k < K; ++k) {
+            const double xv = bio_bf16_to_f64(x[i * K + k]);
+            ss = ss + xv * xv;
+            for (int64_t j = 0; j < N; ++j) {
+                const double p = xv * bio_bf16_to_f64(w[k * N + j]);
+                a[j] = a[j] + p;
+                s[j] = s[j] + fabs(p);
+            }
+        }
+        const double rms = sqrt(ss / (double)K + eps);
+        for (int64_t j = 0; j < N; ++j) {
+            const double val = a[j] / rms;
+            y[i * N + j] = bio_f64_to_f32(val);
+            if (v) v[i * N + j] = val;
+            if (sabs) sabs[i * N + j] = s[j] / rms;
+        }
+    }
+    free(a);
+    free(s);
+    return 0;
+}

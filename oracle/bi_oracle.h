@@ -1,6 +1,7 @@
 /*
  * bi_oracle.h — plain, slow CPU oracle for the batch-invariant GEMM y = x·W
- * (and the batch-invariant RMSNorm and decode attention, declared at the end).
+ * (and the batch-invariant RMSNorm, decode attention and mHC pre-norm projection, declared at
+ * the end).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
  * CPU-baseline leg may load this library.  The product path (the CUDA library and
@@ -102,6 +103,20 @@ int bio_attention_bf16(const uint16_t* q, int64_t T, int64_t Hq, int64_t D,
                        const uint16_t* k_cache, const uint16_t* v_cache, int64_t num_pages,
                        int64_t page_size, int64_t Hkv, const int32_t* page_table, int64_t B,
                        int64_t max_pages, double scale, uint16_t* o, double* v, double* a, double* e);
+
+/* Pre-norm projection of the hyper-connection ("mHC") block ("[BI][DSv4] Make mHC tilelang ops
+ * batch invariant": the prenorm GEMM that projects the flattened streams, with its fused
+ * RMSNorm): for each row i of x[M,K] (bf16 patterns) and W[K,N] (bf16 patterns), in fp64,
+ *
+ *     a[i,j] = sum_{k ascending} x[i,k] * W[k,j]
+ *     ss[i]  = sum_{k ascending} x[i,k]^2
+ *     v[i,j] = a[i,j] / sqrt(ss[i] / K + eps)        (RMSNorm(x_i) . W, no norm weight)
+ *     y[i,j] = RNE fp32 of v[i,j]                     (uint32 patterns)
+ *
+ * Optional fp64 outputs: v (unrounded) and sabs[i,j] = (sum_k |x W|) / sqrt(ss/K + eps), the
+ * scale of the rounding errors.  Returns -1 on a bad argument (sizes, NaN or negative eps). */
+int bio_prenorm_gemm(const uint16_t* x, int64_t M, int64_t K, const uint16_t* w, int64_t N, double eps,
+                     uint32_t* y, double* v, double* sabs);
 
 #ifdef __cplusplus
 }

@@ -145,3 +145,25 @@ def bf16_bits_of_signed_sqrt(q: Fraction, negative: bool) -> int:
             b += 1
         else:
             return sb | b
+
+
+def f32_bits_of_signed_sqrt(q: Fraction, negative: bool) -> int:
+    """Bits of RNE_fp32(+-sqrt(q)) for a rational q >= 0, decided exactly as for bf16 above (the
+    fp32 value whose rounding interval holds sqrt(q), by comparing q with squared midpoints).
+    Finite normal results only."""
+    assert q >= 0
+    sb = 0x80000000 if negative else 0
+    if q == 0:
+        return sb
+    b = to_f32_bits_exact(Fraction(float(q) ** 0.5)) & 0x7FFFFFFF
+    assert 0x00800000 <= b < 0x7F800000
+    while True:
+        v = f32_value(b)
+        lo = (f32_value(b - 1) + v) / 2
+        hi = (v + f32_value(b + 1)) / 2
+        if q < lo * lo or (q == lo * lo and b % 2 == 1):
+            b -= 1
+        elif q > hi * hi or (q == hi * hi and b % 2 == 1):
+            b += 1
+        else:
+            return sb | b
