@@ -560,6 +560,23 @@ def measure_other_paths(dev, peaks):
     g.close()
     out["rmsnorm"] = measure_rmsnorm(dev, peaks, bf)
     out["attention_decode"] = measure_attention(dev, peaks)
+    # mHC pre-norm projection (RMSNorm of the flattened streams times W), fp32 out
+    from invariant_bi_gemm_gb300 import BiPreNorm
+    K, N = 16384, 24
+    W = bf(ig.normal_bf16(ig.SEED_W, K, N, std=0.02))
+    X = bf(ig.scaled_rows_bf16(ig.SEED_X, 256, K))
+    h = BiPreNorm(K, N, 1e-6)
+    rows = []
+    for M in (1, 16, 64, 128, 256):
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        t = timeit(lambda: h(X[:M], W, y))
+        by = 2 * M * K + 2 * K * N + 4 * M * N
+        rows.append({"M": M, "us": round(t * 1e6, 2), "gbs": round(by / t / 1e9, 1),
+                     "frac_hbm": round(by / (peaks["hbm_gbs"] * 1e9) / t, 3)})
+    out["prenorm_mhc"] = {"shape": "RMSNorm(x[M,16384]) . W[16384,24], bf16 in, fp32 out, chunk 512 (32 splits)",
+                          "config": h.config, "rows": rows,
+                          "note": "graph-timed, warm L2 (operands < 10 MB); two kernels per call; latency-bound"}
+    h.close()
     return out
 
 
@@ -724,6 +741,35 @@ def run_attention_only(args):
         sys.exit(1)
 
 
+def run_prenorm_only(args):
+    """Launch only the mHC pre-norm projection (K = 16384, N = 24) at one M, eagerly: --warmup +
+    --steps calls.  For profiling; prints the average call time as one JSON line."""
+    import numpy as np
+    import torch
+
+    import inputgen as ig
+    from invariant_bi_gemm_gb300 import BiPreNorm
+
+    dev = torch.device("cuda", 0)
+    M, K, N = args.prenorm_only_m, 16384, 24
+    x = torch.from_numpy(ig.scaled_rows_bf16(ig.SEED_X, M, K).view(np.int16)).to(dev).view(torch.bfloat16)
+    w = torch.from_numpy(ig.normal_bf16(ig.SEED_W, K, N, std=0.02).view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    h = BiPreNorm(K, N, 1e-6)
+    for _ in range(args.warmup):
+        h(x, w, y)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        h(x, w, y)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / max(1, args.steps)
+    print(json.dumps({"prenorm_only_m": M, "us_per_call": round(t * 1e6, 2)}))
+    h.close()
+
+
 def run_rmsnorm_only(args):
     """Launch only the RMSNorm (d = 4096) at one M, eagerly: --warmup + --steps launches.  For
     profiling; prints the average launch time as one JSON line (not the benchmark line)."""
@@ -802,6 +848,8 @@ def main():
                     help="time a single M of the sweep only (for profiling); skips e2e, paths, CPU")
     ap.add_argument("--attention-only", default="",
                     help="profiling aid: 'B,L' launches only the decode attention for batch B, context L, and exits")
+    ap.add_argument("--prenorm-only-m", type=int, default=0,
+                    help="profiling aid: launch only the mHC pre-norm projection at this M, eagerly, and exit")
     ap.add_argument("--rmsnorm-only-m", type=int, default=0,
                     help="profiling aid: launch only the RMSNorm (d = 4096) at this M, eagerly, and exit")
     ap.add_argument("--mxfp8-only-m", type=int, default=0,
@@ -815,6 +863,9 @@ def main():
         return
     if args.attention_only:
         run_attention_only(args)
+        return
+    if args.prenorm_only_m:
+        run_prenorm_only(args)
         return
     if args.only_m:
         global M_SWEEP

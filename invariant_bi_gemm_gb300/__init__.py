@@ -41,6 +41,8 @@ EXPORTED_SYMBOLS = (
 )
 # every symbol include/bi_rmsnorm.h declares
 RMSNORM_EXPORTED_SYMBOLS = ("bi_rmsnorm_create", "bi_rmsnorm_run", "bi_rmsnorm_get_config", "bi_rmsnorm_destroy")
+# every symbol include/bi_prenorm.h declares
+PRENORM_EXPORTED_SYMBOLS = ("bi_prenorm_create", "bi_prenorm_run", "bi_prenorm_get_config", "bi_prenorm_destroy")
 # every symbol include/bi_attention.h declares
 ATTENTION_EXPORTED_SYMBOLS = ("bi_attention_create", "bi_attention_run", "bi_attention_workspace_size",
                               "bi_attention_get_device_error", "bi_attention_get_config", "bi_attention_destroy")
@@ -75,6 +77,10 @@ class bi_attention_config(ctypes.Structure):
                                               "threads", "stage_positions", "max_ctas", "num_sms")]
 
 
+class bi_prenorm_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("K", "N", "chunk", "splits", "tile_rows")]
+
+
 def _load() -> ctypes.CDLL:
     path = _build.lib_path("libbi_gemm.so")
     if not os.path.exists(path):
@@ -104,9 +110,13 @@ def _load() -> ctypes.CDLL:
     L.bi_attention_get_device_error.argtypes = [P, P]
     L.bi_attention_get_config.argtypes = [P, ctypes.POINTER(bi_attention_config)]
     L.bi_attention_destroy.argtypes = [P]
+    L.bi_prenorm_create.argtypes = [ctypes.POINTER(P), I64, I64, ctypes.c_float, I64]
+    L.bi_prenorm_run.argtypes = [P, P, I64, P, P, P]
+    L.bi_prenorm_get_config.argtypes = [P, ctypes.POINTER(bi_prenorm_config)]
+    L.bi_prenorm_destroy.argtypes = [P]
     for n in ("bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_run_noalloc", "bi_gemm_get_device_error",
               "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_version") + \
-            RMSNORM_EXPORTED_SYMBOLS + ATTENTION_EXPORTED_SYMBOLS:
+            RMSNORM_EXPORTED_SYMBOLS + ATTENTION_EXPORTED_SYMBOLS + PRENORM_EXPORTED_SYMBOLS:
         getattr(L, n).restype = I32
     return L
 
@@ -251,6 +261,29 @@ def bi_attention_get_device_error(h: int, stream: int = 0) -> int:
 
 def bi_attention_destroy(h: int) -> None:
     _check(library().bi_attention_destroy(ctypes.c_void_p(h)), "bi_attention_destroy")
+
+
+def bi_prenorm_create(K: int, N: int, eps: float, chunk: int = 0) -> int:
+    """Returns the handle (an opaque integer); raises BiGemmError on refusal."""
+    h = ctypes.c_void_p()
+    _check(library().bi_prenorm_create(ctypes.byref(h), int(K), int(N), float(eps), int(chunk)), "bi_prenorm_create")
+    return h.value
+
+
+def bi_prenorm_run(h: int, x: int, M: int, W: int, y: int, stream: int) -> None:
+    """Raw-pointer call: x, W, y device addresses, stream a cudaStream_t value."""
+    V = ctypes.c_void_p
+    _check(library().bi_prenorm_run(V(h), V(x), int(M), V(W), V(y), V(stream)), "bi_prenorm_run")
+
+
+def bi_prenorm_get_config(h: int) -> dict:
+    c = bi_prenorm_config()
+    _check(library().bi_prenorm_get_config(ctypes.c_void_p(h), ctypes.byref(c)), "bi_prenorm_get_config")
+    return {n: getattr(c, n) for n, _ in bi_prenorm_config._fields_}
+
+
+def bi_prenorm_destroy(h: int) -> None:
+    _check(library().bi_prenorm_destroy(ctypes.c_void_p(h)), "bi_prenorm_destroy")
 
 
 # --------------------------------------------------------------------- torch wrappers
@@ -449,7 +482,54 @@ class BiAttention:
             pass
 
 
+class BiPreNorm:
+    """mHC pre-norm projection y = RMSNorm(x) . W (fp32 out) on torch tensors: x [M, K] bf16,
+    W [K, N] bf16 (a norm weight folded into W's rows)."""
+
+    def __init__(self, K: int, N: int, eps: float = 1e-6, chunk: int = 0):
+        self.K, self.N, self.eps = int(K), int(N), float(eps)
+        self.handle = bi_prenorm_create(self.K, self.N, self.eps, chunk)
+
+    @property
+    def config(self) -> dict:
+        return bi_prenorm_get_config(self.handle)
+
+    def run(self, x, W, y=None, stream=None):
+        import torch
+        if x.dim() != 2 or x.shape[1] != self.K or tuple(W.shape) != (self.K, self.N):
+            raise ValueError("shape mismatch: x [M, K], W [K, N] expected")
+        if x.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+            raise ValueError("bf16 inputs expected")
+        if not (x.is_cuda and W.is_cuda and x.is_contiguous() and W.is_contiguous()):
+            raise ValueError("x and W must be contiguous CUDA tensors")
+        M = int(x.shape[0])
+        if y is None:
+            y = torch.empty((M, self.N), dtype=torch.float32, device=x.device)
+        if tuple(y.shape) != (M, self.N) or y.dtype != torch.float32 or not y.is_contiguous():
+            raise ValueError("y must be a contiguous [M, N] fp32 tensor")
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        bi_prenorm_run(self.handle, x.data_ptr(), M, W.data_ptr(), y.data_ptr(), s)
+        return y
+
+    __call__ = run
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            bi_prenorm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 __all__ = [
+    "BiPreNorm", "bi_prenorm_create", "bi_prenorm_run", "bi_prenorm_get_config", "bi_prenorm_destroy",
+    "bi_prenorm_config", "PRENORM_EXPORTED_SYMBOLS",
     "BiAttention", "bi_attention_create", "bi_attention_run", "bi_attention_get_config", "bi_attention_workspace_size",
     "bi_attention_get_device_error", "bi_attention_destroy", "bi_attention_config", "ATTENTION_EXPORTED_SYMBOLS",
     "BiRmsNorm", "bi_rmsnorm_create", "bi_rmsnorm_run", "bi_rmsnorm_get_config", "bi_rmsnorm_destroy",

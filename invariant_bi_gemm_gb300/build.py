@@ -1,7 +1,8 @@
 """Build the CUDA libraries in-tree with nvcc for sm_103a.
 
 Produces, under ``invariant_bi_gemm_gb300/_build/``:
-  libbi_gemm.so           the product (C ABI of include/bi_gemm.h, bi_rmsnorm.h, bi_attention.h)
+  libbi_gemm.so           the product (C ABI of include/bi_gemm.h, bi_rmsnorm.h, bi_attention.h,
+                          bi_prenorm.h)
   libbi_gemm_controls.so  test-only negative controls and failure injection
 
 Both are compiled in parallel; a library is rebuilt when any source is newer.
@@ -21,7 +22,7 @@ OUT = os.path.join(PKG, "_build")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 TARGETS = {
-    "libbi_gemm.so": ("bi_gemm.cu", "bi_rmsnorm.cu", "bi_attention.cu"),
+    "libbi_gemm.so": ("bi_gemm.cu", "bi_rmsnorm.cu", "bi_attention.cu", "bi_prenorm.cu"),
     "libbi_gemm_controls.so": ("bi_gemm_controls.cu",),
 }
 

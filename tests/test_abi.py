@@ -94,6 +94,38 @@ def test_attention_null_arguments():
     assert L.bi_attention_destroy(None) == bg.BI_GEMM_OK
 
 
+def test_prenorm_header_symbols_exported():
+    declared = _declared("bi_prenorm.h")
+    assert set(declared) == set(bg.PRENORM_EXPORTED_SYMBOLS)
+    L = ctypes.CDLL(bgbuild.lib_path("libbi_gemm.so"))
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+@pytest.mark.parametrize("K,N,eps,chunk,want", [
+    (16384, 24, -1.0, 0, bg.BI_GEMM_ERR_INVALID_ARG),
+    (16384, 24, float("nan"), 0, bg.BI_GEMM_ERR_INVALID_ARG),
+    (16384, 24, 1e-6, -64, bg.BI_GEMM_ERR_INVALID_ARG),
+    (16380, 24, 1e-6, 0, bg.BI_GEMM_ERR_UNSUPPORTED),     # K not a whole number of 16-byte pieces
+    (16384, 20, 1e-6, 0, bg.BI_GEMM_ERR_UNSUPPORTED),     # N % 8
+    (16384, 40, 1e-6, 0, bg.BI_GEMM_ERR_UNSUPPORTED),     # N > 32
+    (16384, 24, 1e-6, 96, bg.BI_GEMM_ERR_UNSUPPORTED),    # chunk % 64
+    (16384, 24, 1e-6, 2048, bg.BI_GEMM_ERR_UNSUPPORTED),
+])
+def test_prenorm_create_refuses_before_touching_cuda(K, N, eps, chunk, want):
+    h = ctypes.c_void_p()
+    assert bg.library().bi_prenorm_create(ctypes.byref(h), K, N, eps, chunk) == want
+    assert h.value is None
+
+
+def test_prenorm_null_arguments():
+    L = bg.library()
+    assert L.bi_prenorm_create(None, 16384, 24, 1e-6, 0) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_prenorm_run(None, None, 4, None, None, None) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_prenorm_get_config(None, None) == bg.BI_GEMM_ERR_INVALID_ARG
+    assert L.bi_prenorm_destroy(None) == bg.BI_GEMM_OK
+
+
 def test_controls_symbols_exported():
     declared = _declared("bi_gemm_controls.h")
     assert declared, "controls header declares nothing"
