@@ -56,10 +56,13 @@ typedef struct bi_attention* bi_attention_t;
 typedef struct {
   int32_t num_q_heads, num_kv_heads, head_dim, page_size;
   int32_t split_size;       /* positions per split (fixed for the handle)                      */
-  int32_t threads;          /* threads per block (one block per (token, KV head, split) unit) */
+  int32_t threads;          /* threads per block of the attention kernel                      */
   int32_t stage_positions;  /* positions staged in shared memory at a time                    */
   int32_t max_ctas;         /* persistent grid bound: resident blocks per SM x SMs            */
   int32_t num_sms;
+  int32_t tma_pages;        /* 1: pages are loaded as TMA boxes by a producer warp (page sizes
+                               8, 16, 32, 64); 0: rows are copied by every thread (cp.async)  */
+  int32_t ring_stages;      /* depth of the staging ring                                       */
 } bi_attention_config;
 
 /* Create a handle.  Requirements (else BI_GEMM_ERR_UNSUPPORTED): head_dim 64 or 128;
@@ -75,7 +78,15 @@ int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, int64_t num_kv
  * grows the handle's workspace (stream-ordered cudaMallocAsync) when T or max_pos outgrow it
  * (BI_GEMM_ERR_OOM if that fails), then queues three kernels on `stream`: a plan of the
  * (token, KV head, split) units, the attention of every unit, and the merge of the splits of
- * tokens that have more than one.  Asynchronous. */
+ * tokens that have more than one.  Asynchronous.
+ *
+ * Two attention kernels, with the same arithmetic and the same bits: for page sizes 8, 16, 32
+ * and 64 (a 64-position stage is whole pages) a producer warp loads every page's rows of a KV
+ * head as 3-D TMA boxes into a ring that runs ahead across units, and four warps compute; for
+ * other page sizes (or a cache of 2^31 rows or more) every thread copies 16-byte row chunks
+ * with cp.async.  The waits of the TMA kernel on its ring are bounded (2 s): past the limit the
+ * block stops, its output is undefined and bi_attention_get_device_error reports
+ * BI_GEMM_ERR_TIMEOUT. */
 int bi_attention_run(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,
                      const int32_t* q_pos, const void* k_cache, const void* v_cache,
                      int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
@@ -84,8 +95,9 @@ int bi_attention_run(bi_attention_t h, const void* q, int64_t T, const int32_t* 
 /* Workspace bytes a run with T tokens and the bound max_pos needs. */
 int bi_attention_workspace_size(bi_attention_t h, int64_t T, int64_t max_pos, uint64_t* bytes);
 
-/* Synchronise `stream`; BI_GEMM_ERR_INVALID_ARG if a kernel caught a bad input since the last
- * call (then cleared), BI_GEMM_ERR_CUDA if synchronisation failed, else BI_GEMM_OK. */
+/* Synchronise `stream`; BI_GEMM_ERR_TIMEOUT if a bounded wait expired, else
+ * BI_GEMM_ERR_INVALID_ARG if a kernel caught a bad input, since the last call (the status is then
+ * cleared); BI_GEMM_ERR_CUDA if synchronisation failed; else BI_GEMM_OK. */
 int bi_attention_get_device_error(bi_attention_t h, void* stream);
 
 int bi_attention_get_config(bi_attention_t h, bi_attention_config* c);

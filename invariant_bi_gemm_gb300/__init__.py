@@ -74,7 +74,8 @@ class bi_rmsnorm_config(ctypes.Structure):
 
 class bi_attention_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("num_q_heads", "num_kv_heads", "head_dim", "page_size", "split_size",
-                                              "threads", "stage_positions", "max_ctas", "num_sms")]
+                                              "threads", "stage_positions", "max_ctas", "num_sms", "tma_pages",
+                                              "ring_stages")]
 
 
 class bi_prenorm_config(ctypes.Structure):

@@ -20,18 +20,23 @@
 //      merge kernel combines the n splits of each (token, KV head): M = max m_s, then
 //      L = sum l_s 2^(m_s - M) and A = sum acc_s 2^(m_s - M) over four consecutive groups of
 //      splits (ascending within a group, the four group sums added in order), o = A / L.
-// A plan kernel first turns q_pos into per-token unit offsets (a prefix sum) and the token of
+// A plan kernel first turns q_pos into per-token unit offsets (a prefix sum) and a record of
 // every unit.  The attention kernel is persistent: a block fetches its next unit's coordinates,
 // row offsets and query while it works on the current one and issues the next unit's first
 // stages into the ring during the current unit's last ones, so that the key/value stream does
 // not drain between units; with the merge in a kernel of its own a unit ends without any fence
-// or counter.
+// or counter.  For page sizes 8, 16, 32 and 64 a second attention kernel (attn_tma_kernel, below)
+// runs the same arithmetic with the keys and values loaded as TMA page boxes by a producer warp.
+// The attention and merge kernels are programmatic dependents of their predecessors.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "../../include/bi_attention.h"
@@ -63,13 +68,15 @@ struct Params {
   const int32_t* table;
   uint16_t* o;
   int32_t* cum;      // [T + 1] first unit of each token
-  int32_t* umap;     // [units] the token of each unit
+  int4* urec;        // [units] (token, request, position, split * Hkv + KV head) of each unit
   float* part;       // [T * Hkv * max_splits, G, D] partial weighted sums
   float* ml;         // [T * Hkv * max_splits, G, 2] (maximum, sum of weights)
   uint32_t* status;
   int64_t T, num_pages, B, max_pages;
   int32_t Hq, Hkv, page_size, split, max_splits;
   int32_t max_pos;   // the host's bound on q_pos
+  int32_t nstage;    // ring depth of the TMA variant
+  uint64_t timeout_ns;   // limit of its bounded waits
   float c;           // scale * log2(e)
 };
 
@@ -81,19 +88,22 @@ __device__ __forceinline__ float bf16_f(uint16_t b) { return __uint_as_float(uin
 // Number of splits of a token at position p.
 __device__ __forceinline__ int32_t splits_of(int32_t p, int32_t split) { return p / split + 1; }
 
-// Unit offsets: cum[t] = Hkv * (splits of the tokens before t) and the token of every unit; a
-// token with an input the kernel cannot serve gets no units (and sets the status word).
+// Unit offsets: cum[t] = Hkv * (splits of the tokens before t), and the record of every unit
+// (its token, request, position and split * Hkv + KV head); a token with an input the kernel
+// cannot serve gets no units (and sets the status word).
 __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
+  ptx::launch_dependents();   // the attention kernel may start its prologue now
   const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   if (tid == 0) carry = 0;
   __syncthreads();
   for (int64_t base = 0; base < p.T; base += 1024) {
     const int64_t t = base + tid;
-    int32_t n = 0;
+    int32_t n = 0, b = 0, pos = 0;
     if (t < p.T) {
-      const int32_t b = p.q_seq[t], pos = p.q_pos[t];
+      b = p.q_seq[t];
+      pos = p.q_pos[t];
       if (b < 0 || b >= p.B || pos < 0 || int64_t(pos / p.page_size) >= p.max_pages) {
         atomicOr(p.status, kErrInput);
       } else if (pos > p.max_pos) {
@@ -121,9 +131,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
     }
     __syncthreads();
     const int32_t incl = carry + x + (warp > 0 ? warp_sums[warp - 1] : 0);
-    if (t < p.T) {
-      p.cum[t] = incl - n;
-      for (int32_t i = incl - n; i < incl; ++i) p.umap[i] = int32_t(t);
+    if (t < p.T) p.cum[t] = incl - n;
+    // the unit records of the warp's 32 tokens, one token at a time by the whole warp (a long
+    // context has hundreds of units)
+    for (int k = 0; k < 32; ++k) {
+      const int32_t nk = __shfl_sync(0xFFFFFFFFu, n, k);
+      const int32_t sk = __shfl_sync(0xFFFFFFFFu, incl - n, k);
+      const int32_t bk = __shfl_sync(0xFFFFFFFFu, b, k), pk = __shfl_sync(0xFFFFFFFFu, pos, k);
+      const int32_t tk = int32_t(base + warp * 32 + k);
+      for (int32_t r = lane; r < nk; r += 32) p.urec[sk + r] = make_int4(tk, bk, pk, r);
     }
     __syncthreads();
     if (tid == 1023) carry = incl;
@@ -189,14 +205,13 @@ struct Unit {
   int32_t kh, s, pos, nsplit, j0, valid, nsub;
 };
 
-__device__ __forceinline__ Unit unit_of(const Params& p, int64_t u) {
+__device__ __forceinline__ Unit unit_from(const Params& p, const int4 rec) {
   Unit w;
-  w.t = p.umap[u];
-  const int32_t r = int32_t(u - p.cum[w.t]);
-  w.s = r / p.Hkv;
-  w.kh = r - w.s * p.Hkv;
-  w.b = p.q_seq[w.t];
-  w.pos = p.q_pos[w.t];
+  w.t = rec.x;
+  w.b = rec.y;
+  w.pos = rec.z;
+  w.s = rec.w / p.Hkv;
+  w.kh = rec.w - w.s * p.Hkv;
   w.nsplit = splits_of(w.pos, p.split);
   w.j0 = w.s * p.split;
   w.valid = min(p.split, w.pos + 1 - w.j0);                  // keys in this split (>= 1)
@@ -222,6 +237,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
   const bool row_ok = gq < G;
   const int dbase = warp * C::DW;               // this warp's output dimensions
 
+  ptx::grid_dependency_wait();   // the plan is complete and visible
+  ptx::launch_dependents();
   const int32_t total = p.cum[p.T];
   int64_t u = blockIdx.x;
   if (u >= total) return;
@@ -278,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
     return stage + r * C::ROW_BYTES + ((c ^ (r & (C::CHUNKS - 1))) << 4);
   };
 
-  Unit cur = unit_of(p, u);
+  Unit cur = unit_from(p, p.urec[u]);
   int half = 0;
   load_q(cur, half);
   fill_rows(cur, half);
@@ -301,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
     Unit nxt;
     auto fetch_next = [&]() {
       if (has_next) {
-        nxt = unit_of(p, un);
+        nxt = unit_from(p, p.urec[un]);
         fill_rows(nxt, half ^ 1);
         load_q(nxt, half ^ 1);
       }
@@ -451,6 +468,375 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
   if (bad_page) atomicOr(p.status, kErrPage);
 }
 
+// ------------------------------------------------------------------ TMA page-box variant
+// The same unit arithmetic for page sizes 8, 16, 32 and 64, where a 64-position stage is whole
+// pages.  Warp 0 is a producer: for every page of a stage it loads the rows of the unit's KV
+// head as [page_size x 64] boxes (two per page for a head dimension of 128) with 3-D TMA,
+// 128-byte swizzled, into a ring of stages and runs ahead across units; a page index outside
+// the cache loads a box from past the cache's end, which TMA fills with zeros (the rows the
+// row-copy kernel zero-fills).  Warps 1..4 compute exactly as attn_kernel's four warps do (same
+// instructions in the same order on the same values), so both kernels give the same bits.  Both
+// roles read the next unit's record one unit ahead (the producer also its page-table entries,
+// the consumers its query rows), so that no dependent load stalls the stream at a unit change.
+// Every wait on the ring is bounded: past the limit the block sets kErrTimeout, stops issuing,
+// waits (bounded) for the copies it has in flight, and leaves.
+constexpr int kConsumers = 4;                 // consumer warps: attn_kernel's layout
+constexpr int kTmaThreads = 32 + kThreads;    // producer warp + consumers
+constexpr int kTmaBlocksPerSm = 3;            // the ring depth is sized for three blocks per SM
+constexpr int kTmaMaxStages = 8;
+constexpr uint32_t kErrTimeout = 8u;          // a bounded wait on the ring expired
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+template <int D, int G>
+struct TmaCfg {
+  using C = Cfg<D, G>;
+  static constexpr int HALVES = D / 64;                // 128-byte column halves of a row
+  static constexpr int HALF_BYTES = kStagePos * 128;   // one half of a stage: 64 rows of 128 B
+  static constexpr int STAGE_BYTES = HALVES * HALF_BYTES;
+  static constexpr int QW = (G * D / 2 + kThreads - 1) / kThreads;   // query words per consumer
+  // 1024-byte alignment slack | ring [nstage] | full, empty barriers [nstage] each | scores
+  // [G][stride] | per-warp maxima, sums [G][4] each | maximum, sum [G] each | query rows [G][QS]
+  __host__ __device__ static size_t fixed_bytes(int split) {
+    return 1024 + sizeof(float) * (size_t(G) * C::sc_stride(split) + G * 10) + sizeof(uint16_t) * G * C::QS;
+  }
+  static size_t smem_bytes(int split, int nstage) { return fixed_bytes(split) + size_t(nstage) * (STAGE_BYTES + 16); }
+};
+
+// Bounded wait for a phase of a ring barrier: false (status set, block aborted) past the time
+// limit, or at once once another role of the block has aborted.
+__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, const Params& p, volatile uint32_t* abort) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (ptx::globaltimer() - t0 > p.timeout_ns) {
+      atomicOr(p.status, kErrTimeout);
+      *abort = 1u;
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
+    attn_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Params p) {
+  using C = Cfg<D, G>;
+  using TC = TmaCfg<D, G>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const int NS = p.nstage;
+  const int SCS = C::sc_stride(p.split);
+  const uint32_t bars = sbase + uint32_t(NS * TC::STAGE_BYTES);   // full [NS], then empty [NS]
+  float* sc = reinterpret_cast<float*>(smem + NS * TC::STAGE_BYTES + 16 * NS);   // [G][SCS]
+  float* red = sc + G * SCS;
+  float* redl = red + G * 4;
+  float* hm = redl + G * 4;
+  float* hl = hm + G;
+  uint16_t* qsm = reinterpret_cast<uint16_t*>(hl + G);   // [G][QS]
+  __shared__ uint32_t s_abort;
+  volatile uint32_t* abort = &s_abort;
+  const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_abort = 0u;
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(bars + 8 * s, 1);
+      ptx::mbar_init(bars + 8 * (NS + s), kConsumers);
+    }
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&tmk);
+    ptx::prefetch_tensormap(&tmv);
+  }
+  __syncthreads();
+  ptx::grid_dependency_wait();   // the plan is complete and visible
+  ptx::launch_dependents();
+  const int32_t total = p.cum[p.T];
+  if (int64_t(blockIdx.x) >= total) return;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const int ps = p.page_size;
+    const int ppst = kStagePos / ps;                   // pages per stage: 1, 2, 4 or 8
+    const uint32_t box_bytes = uint32_t(ps) * 128;
+    const int32_t past_end = int32_t(p.num_pages * ps);   // a row coordinate past the cache
+    // page-table entries of a unit: lane l holds those of its pages l, l + 32, l + 64, l + 96
+    auto load_pages = [&](const Unit& w, int32_t (&pg)[4]) {
+      const int npu = (w.valid + ps - 1) / ps;
+      const int32_t* row = p.table + w.b * p.max_pages + w.j0 / ps;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pg[k] = lane + 32 * k < npu ? row[lane + 32 * k] : -1;
+    };
+    bool bad_page = false, stop = false;
+    uint32_t seq = 0;   // loads issued
+    int64_t u = blockIdx.x;
+    Unit cur = unit_from(p, p.urec[u]);
+    int32_t pg[4];
+    load_pages(cur, pg);
+    while (!stop) {
+      const int64_t un = u + gridDim.x;
+      const bool has_next = un < total;
+      int4 nrec = make_int4(0, 0, 0, 0);
+      Unit nxt = cur;
+      int32_t npg[4] = {-1, -1, -1, -1};
+      const int nload = 2 * cur.nsub;
+      const int npu = (cur.valid + ps - 1) / ps;
+      for (int i = 0; i < nload; ++i, ++seq) {
+        if (i == 0 && has_next) nrec = p.urec[un];
+        if (i == 1 && has_next) {
+          nxt = unit_from(p, nrec);
+          load_pages(nxt, npg);
+        }
+        const int slot = int(seq % uint32_t(NS));
+        const uint32_t round = seq / uint32_t(NS);
+        bool ok = true;
+        if (lane == 0 && round > 0) ok = ring_wait(bars + 8 * (NS + slot), (round - 1) & 1u, p, abort);
+        if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) {
+          stop = true;
+          break;
+        }
+        const bool isv = i >= cur.nsub;
+        const int sub = isv ? i - cur.nsub : i;
+        const int idx0 = sub * ppst;                     // first page of the stage in the unit
+        const int cnt = min(ppst, npu - idx0);           // pages of the stage that hold keys
+        const uint32_t full = bars + 8 * slot;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(full, uint32_t(cnt * TC::HALVES) * box_bytes);
+        __syncwarp();
+        const int k = idx0 >> 5, l0 = idx0 & 31;         // a stage's pages sit in one register
+        if (lane >= l0 && lane < l0 + cnt) {
+          const int32_t page = k == 0 ? pg[0] : k == 1 ? pg[1] : k == 2 ? pg[2] : pg[3];
+          int32_t row = past_end;
+          if (page >= 0 && int64_t(page) < p.num_pages) row = page * ps;
+          else bad_page = true;
+          const uint32_t dst = sbase + uint32_t(slot * TC::STAGE_BYTES) + uint32_t(lane - l0) * box_bytes;
+#pragma unroll
+          for (int hh = 0; hh < TC::HALVES; ++hh)
+            ptx::tma_load_3d(dst + hh * TC::HALF_BYTES, isv ? &tmv : &tmk, full, hh * 64, cur.kh, row);
+        }
+      }
+      if (stop || !has_next) break;
+      cur = nxt;
+      u = un;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pg[k] = npg[k];
+    }
+    if (bad_page) atomicOr(p.status, kErrPage);
+    // the block must not leave while a copy into its shared memory is in flight: wait (bounded)
+    // for the latest load of every slot
+    if (lane == 0) {
+      for (uint32_t k = 0; k < uint32_t(NS) && k < seq; ++k) {
+        const uint32_t q = seq - 1 - k;
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(bars + 8 * (q % uint32_t(NS)), (q / uint32_t(NS)) & 1u)) {
+          if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            atomicOr(p.status, kErrTimeout);
+            break;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int ctid = tid - 32, cw = warp - 1;
+  const int gq = lane >> 2, tq = lane & 3;
+  const bool row_ok = gq < G;
+  const int dbase = cw * C::DW;
+  // 16-byte chunk c of staged row r (the boxes' 128-byte swizzle: two column halves of 64 rows)
+  auto chunk_addr = [&](uint32_t stage, int r, int c) {
+    return stage + uint32_t((c >> 3) * TC::HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  };
+  auto load_q = [&](const Unit& w, uint32_t (&qr)[TC::QW]) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q + (w.t * p.Hq + int64_t(w.kh) * G) * D);
+#pragma unroll
+    for (int k = 0; k < TC::QW; ++k) {
+      const int i = ctid + k * kThreads;
+      qr[k] = i < G * D / 2 ? src[i] : 0u;
+    }
+  };
+  int64_t u = blockIdx.x;
+  Unit cur = unit_from(p, p.urec[u]);
+  uint32_t qr[TC::QW];
+  load_q(cur, qr);
+  uint32_t seq = 0;
+  bool ok = true;   // false once a wait gave up: the warp then skips the work but walks the barriers
+  while (true) {
+    {
+      uint32_t* dst = reinterpret_cast<uint32_t*>(qsm);
+#pragma unroll
+      for (int k = 0; k < TC::QW; ++k) {
+        const int i = ctid + k * kThreads;
+        if (i < G * D / 2) dst[(i / (D / 2)) * (C::QS / 2) + i % (D / 2)] = qr[k];
+      }
+    }
+    ptx::named_bar_sync1<kThreads>();
+    // this thread's query A fragments for every k step, held for the unit:
+    // qa[k][0] = q[gq][16k + 2tq, +1], qa[k][1] = q[gq][16k + 8 + 2tq, +1] (zero past the G heads)
+    uint32_t qa[C::KSTEPS][2];
+    {
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qsm + (row_ok ? gq : 0) * C::QS);
+#pragma unroll
+      for (int k = 0; k < C::KSTEPS; ++k) {
+        qa[k][0] = row_ok ? qrow[8 * k + tq] : 0u;
+        qa[k][1] = row_ok ? qrow[8 * k + 4 + tq] : 0u;
+      }
+    }
+    const int64_t un = u + gridDim.x;
+    const bool has_next = un < total;
+    int4 nrec = make_int4(0, 0, 0, 0);
+    Unit nxt = cur;
+    const int nload = 2 * cur.nsub;
+    float acc[C::NT2][4];
+#pragma unroll
+    for (int n = 0; n < C::NT2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+    for (int i = 0; i < nload; ++i, ++seq) {
+      if (i == 0 && has_next) nrec = p.urec[un];
+      if (i == 1 && has_next) {
+        nxt = unit_from(p, nrec);
+        load_q(nxt, qr);
+      }
+      const int slot = int(seq % uint32_t(NS));
+      if (ok && !ring_wait(bars + 8 * slot, (seq / uint32_t(NS)) & 1u, p, abort)) ok = false;
+      ok = __all_sync(0xFFFFFFFFu, ok);   // the warp's MMAs run with all lanes or none
+      const uint32_t stage = sbase + uint32_t(slot * TC::STAGE_BYTES);
+      if (i < cur.nsub) {
+        if (ok) {
+          const int pos0 = i * kStagePos + cw * (kStagePos / 4);
+#pragma unroll
+          for (int nt = 0; nt < C::NT1; ++nt) {
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const int prow = cw * (kStagePos / 4) + nt * 8 + (lane & 7);
+#pragma unroll
+            for (int kp = 0; kp < C::KSTEPS / 2; ++kp) {
+              uint32_t b[4];
+              ldsm_x4(chunk_addr(stage, prow, 4 * kp + (lane >> 3)), b);
+              mma16816(d, qa[2 * kp][0], qa[2 * kp][1], b[0], b[1]);
+              mma16816(d, qa[2 * kp + 1][0], qa[2 * kp + 1][1], b[2], b[3]);
+            }
+            const int jl = pos0 + nt * 8 + 2 * tq;
+            if (row_ok) {
+              if (jl < cur.valid) sc[gq * SCS + jl] = __fmul_rn(d[0], p.c);
+              if (jl + 1 < cur.valid) sc[gq * SCS + jl + 1] = __fmul_rn(d[1], p.c);
+            }
+          }
+        }
+        if (i == cur.nsub - 1) {
+          ptx::named_bar_sync1<kThreads>();
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float m = -INFINITY;
+            for (int jj = ctid; jj < cur.valid; jj += kThreads) m = fmaxf(m, sc[g * SCS + jj]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if (lane == 0) red[g * 4 + cw] = m;
+          }
+          ptx::named_bar_sync1<kThreads>();
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float m = fmaxf(fmaxf(red[g * 4 + 0], red[g * 4 + 1]), fmaxf(red[g * 4 + 2], red[g * 4 + 3]));
+            float ls = 0.0f;
+            for (int jj = ctid; jj < cur.valid; jj += kThreads) {
+              const float w = exp2f(__fsub_rn(sc[g * SCS + jj], m));
+              sc[g * SCS + jj] = w;
+              ls = __fadd_rn(ls, w);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xFFFFFFFFu, ls, o));
+            if (ctid == 0) hm[g] = m;
+            if (lane == 0) redl[g * 4 + cw] = ls;
+          }
+          ptx::named_bar_sync1<kThreads>();
+          if (ctid < G)
+            hl[ctid] = __fadd_rn(__fadd_rn(__fadd_rn(redl[ctid * 4 + 0], redl[ctid * 4 + 1]), redl[ctid * 4 + 2]),
+                                 redl[ctid * 4 + 3]);
+        }
+      } else {
+        const int sub = i - cur.nsub;
+        const int rows = min(kStagePos, cur.valid - sub * kStagePos);
+        if (rows & 15) {
+          // the value rows the last 16-position step reads past the split's keys (another
+          // request's slots of a partly used page, or an earlier stage) become zeros: they meet
+          // zero weights, as the zero-filled rows of attn_kernel do
+          if (ok) {
+            const int r0 = rows, nr = ((rows + 15) & ~15) - rows;
+            for (int e = ctid; e < nr * (D / 8); e += kThreads)
+              ptx::st_shared_v4(chunk_addr(stage, r0 + e / (D / 8), e % (D / 8)), 0u, 0u, 0u, 0u);
+            ptx::fence_proxy_async_smem();   // ordered before the slot's next TMA write
+          }
+          ptx::named_bar_sync1<kThreads>();
+        }
+        if (ok) {
+          for (int k0 = 0; k0 < rows; k0 += 16) {
+            // weights of positions jb, jb + 1, jb + 8, jb + 9 (zero past the split's keys)
+            const int jb = sub * kStagePos + k0 + 2 * tq;
+            const float* srow = sc + (row_ok ? gq : 0) * SCS;
+            const float2 w0 = *reinterpret_cast<const float2*>(srow + jb);
+            const float2 w1 = *reinterpret_cast<const float2*>(srow + jb + 8);
+            float pw[4] = {w0.x, w0.y, w1.x, w1.y};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (!row_ok || jb + (e >> 1) * 8 + (e & 1) >= cur.valid) pw[e] = 0.0f;
+            uint32_t ah[2], al[2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const float x0 = pw[2 * h2], x1 = pw[2 * h2 + 1];
+              ah[h2] = pack_bf16x2(x0, x1);
+              const float h0 = __uint_as_float(ah[h2] << 16), h1 = __uint_as_float(ah[h2] & 0xFFFF0000u);
+              al[h2] = pack_bf16x2(__fsub_rn(x0, h0), __fsub_rn(x1, h1));
+            }
+#pragma unroll
+            for (int np = 0; np < C::NT2 / 2; ++np) {
+              uint32_t b[4];
+              const int prow = k0 + ((lane >> 3) & 1) * 8 + (lane & 7);
+              ldsm_x4_trans(chunk_addr(stage, prow, (dbase + 16 * np) / 8 + (lane >> 4)), b);
+              mma16816(acc[2 * np], ah[0], ah[1], b[0], b[1]);
+              mma16816(acc[2 * np], al[0], al[1], b[0], b[1]);
+              mma16816(acc[2 * np + 1], ah[0], ah[1], b[2], b[3]);
+              mma16816(acc[2 * np + 1], al[0], al[1], b[2], b[3]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bars + 8 * (NS + slot));   // this warp is done with the slot
+    }
+
+    ptx::named_bar_sync1<kThreads>();   // hl is written
+    if (ok) {
+      const int64_t orow = (cur.t * p.Hq + int64_t(cur.kh) * G + gq) * D;
+      if (cur.nsplit == 1) {
+        if (row_ok) {
+          const float l = hl[gq];
+#pragma unroll
+          for (int n = 0; n < C::NT2; ++n)
+            *reinterpret_cast<uint32_t*>(p.o + orow + dbase + 8 * n + 2 * tq) =
+                pack_bf16x2(__fdiv_rn(acc[n][0], l), __fdiv_rn(acc[n][1], l));
+        }
+      } else {
+        const int64_t slot = (cur.t * p.Hkv + cur.kh) * int64_t(p.max_splits) + cur.s;
+        if (row_ok) {
+#pragma unroll
+          for (int n = 0; n < C::NT2; ++n)
+            *reinterpret_cast<float2*>(p.part + (slot * G + gq) * D + dbase + 8 * n + 2 * tq) =
+                make_float2(acc[n][0], acc[n][1]);
+        }
+        if (ctid < G) {
+          p.ml[(slot * G + ctid) * 2 + 0] = hm[ctid];
+          p.ml[(slot * G + ctid) * 2 + 1] = hl[ctid];
+        }
+      }
+    }
+    // the scores, per-head values and query rows are reused by the next unit; every consumer
+    // warp takes the same decision to go on
+    if (ptx::named_bar_or1<kThreads>(!ok) || !has_next) break;
+    cur = nxt;
+    u = un;
+  }
+}
+
 // Merge of the splits of every (token, KV head) with more than one split, after all units.  The
 // n splits are cut into four consecutive groups of c = ceil(n / 4); every output pair of every
 // head is handled by four threads, one per group, so that the partial loads of a long split list
@@ -463,6 +849,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
   constexpr int kPairs = G * D / 2;
   __shared__ float sm[kPairs][4];       // group maxima, then group sums of weights
   __shared__ float2 sa[kPairs][4];      // group weighted sums
+  ptx::grid_dependency_wait();   // every unit's partial results are complete and visible
   const int64_t job = blockIdx.x;                       // token * Hkv + KV head
   const int64_t t = job / p.Hkv;
   const int32_t kh = int32_t(job - t * p.Hkv);
@@ -521,14 +908,20 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
 
 struct KernelInfo {
   const void* fn = nullptr;
+  const void* tma = nullptr;
   const void* merge = nullptr;
   size_t (*smem)(int) = nullptr;
+  size_t (*tma_fixed)(int) = nullptr;   // TMA variant: shared memory besides the ring
+  int tma_stage_bytes = 0;
 };
 
 template <int D, int G>
 KernelInfo info() {
   KernelInfo k;
   k.fn = reinterpret_cast<const void*>(&attn_kernel<D, G>);
+  k.tma = reinterpret_cast<const void*>(&attn_tma_kernel<D, G>);
+  k.tma_fixed = &TmaCfg<D, G>::fixed_bytes;
+  k.tma_stage_bytes = TmaCfg<D, G>::STAGE_BYTES;
   k.merge = reinterpret_cast<const void*>(&merge_kernel<D, G>);
   k.smem = &Cfg<D, G>::smem_bytes;
   return k;
@@ -555,6 +948,33 @@ inline KernelInfo select(int D, int G) {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// A cache [rows = num_pages * page_size, Hkv, D] (bf16) as a 3-D tensor, box [page_size, 1, 64]:
+// one page's rows of one KV head and 64 of its dimensions, 128-byte swizzled, zero fill outside.
+bool encode_cache(CUtensorMap* m, const void* base, int64_t rows, int Hkv, int D, int page_size) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(rows)};
+  cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2};
+  cuuint32_t box[3] = {64, 1, cuuint32_t(page_size)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace biattn
 
 struct bi_attention {
@@ -562,6 +982,10 @@ struct bi_attention {
   float scale = 0.0f;
   int device = 0, num_sms = 0, max_ctas = 0;
   size_t smem = 0;
+  // TMA page-box variant (page sizes 8, 16, 32, 64): ring depth, shared memory, grid bound
+  bool tma = false;
+  int nstage = 0, tma_ctas = 0;
+  size_t tma_smem = 0;
   biattn::KernelInfo kern;
   uint32_t* d_status = nullptr;
   void* ws = nullptr;
@@ -571,7 +995,7 @@ struct bi_attention {
 namespace {
 
 struct WsLayout {
-  size_t cum, umap, part, ml, total;
+  size_t cum, urec, part, ml, total;
 };
 
 WsLayout layout_of(const bi_attention* h, int64_t T, int64_t max_pos) {
@@ -579,8 +1003,8 @@ WsLayout layout_of(const bi_attention* h, int64_t T, int64_t max_pos) {
   const int64_t slots = T * h->Hkv * max_splits;
   WsLayout w;
   w.cum = 0;
-  w.umap = biattn::align256(size_t(T + 1) * sizeof(int32_t));
-  w.part = w.umap + biattn::align256(size_t(slots) * sizeof(int32_t));
+  w.urec = biattn::align256(size_t(T + 1) * sizeof(int32_t));
+  w.part = w.urec + biattn::align256(size_t(slots) * sizeof(int4));
   w.ml = w.part + biattn::align256(size_t(slots) * h->G * h->D * sizeof(float));
   w.total = w.ml + biattn::align256(size_t(slots) * h->G * 2 * sizeof(float));
   return w;
@@ -623,8 +1047,42 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
     cudaGetLastError();
     return BI_GEMM_ERR_CUDA;
   }
+  // TMA variant: the deepest ring (up to 8 stages) with which kTmaBlocksPerSm blocks fit on an SM
+  bool tma = false;
+  int nstage = 0, tma_per_sm = 0;
+  size_t tma_smem = 0;
+  if (page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64) {
+    int sm_bytes = 0, reserved = 0, optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, k.tma) != cudaSuccess) {
+      cudaGetLastError();
+      return BI_GEMM_ERR_CUDA;
+    }
+    const int64_t budget = int64_t(sm_bytes) / biattn::kTmaBlocksPerSm - reserved - int64_t(fa.sharedSizeBytes) -
+                           int64_t(k.tma_fixed(int(split)));
+    nstage = int(std::min<int64_t>(biattn::kTmaMaxStages, budget / (k.tma_stage_bytes + 16)));
+    if (nstage >= 2 && biattn::encode_fn()) {
+      tma_smem = k.tma_fixed(int(split)) + size_t(nstage) * (k.tma_stage_bytes + 16);
+      // per kernel, shared by every handle of the head shape: the most a block may have
+      if (cudaFuncSetAttribute(k.tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               optin - int(fa.sharedSizeBytes)) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&tma_per_sm, k.tma, biattn::kTmaThreads, tma_smem) !=
+              cudaSuccess) {
+        cudaGetLastError();
+        return BI_GEMM_ERR_CUDA;
+      }
+      tma = tma_per_sm >= 1;
+    }
+  }
   bi_attention* h = new (std::nothrow) bi_attention();
   if (!h) return BI_GEMM_ERR_OOM;
+  h->tma = tma;
+  h->nstage = tma ? nstage : 0;
+  h->tma_smem = tma_smem;
+  h->tma_ctas = tma_per_sm * sms;
   h->Hq = int(num_q_heads);
   h->Hkv = int(num_kv_heads);
   h->D = int(head_dim);
@@ -701,7 +1159,7 @@ BI_GEMM_API int bi_attention_run(bi_attention_t h, const void* q, int64_t T, con
   p.table = page_table;
   p.o = static_cast<uint16_t*>(o);
   p.cum = reinterpret_cast<int32_t*>(ws + w.cum);
-  p.umap = reinterpret_cast<int32_t*>(ws + w.umap);
+  p.urec = reinterpret_cast<int4*>(ws + w.urec);
   p.part = reinterpret_cast<float*>(ws + w.part);
   p.ml = reinterpret_cast<float*>(ws + w.ml);
   p.status = h->d_status;
@@ -716,14 +1174,48 @@ BI_GEMM_API int bi_attention_run(bi_attention_t h, const void* q, int64_t T, con
   p.max_splits = int32_t(max_pos / h->split + 1);
   p.max_pos = int32_t(max_pos);
   p.c = h->scale * 1.4426950408889634f;   // log2(e)
+  p.nstage = h->nstage;
+  p.timeout_ns = biattn::kTimeoutNs;
+  // The TMA variant needs the caches' rows addressable by int32 box coordinates (one page past
+  // the end included); otherwise, or if a tensor map cannot be encoded, the row-copy kernel
+  // runs: both give the same bits.
+  CUtensorMap tmk, tmv;
+  const int64_t rows = num_pages * h->page_size;
+  const bool use_tma = h->tma && num_pages > 0 && rows + h->page_size < (int64_t(1) << 31) &&
+                       biattn::encode_cache(&tmk, k_cache, rows, h->Hkv, h->D, h->page_size) &&
+                       biattn::encode_cache(&tmv, v_cache, rows, h->Hkv, h->D, h->page_size);
   biattn::plan_kernel<<<1, 1024, 0, st>>>(p);
   if (cudaGetLastError() != cudaSuccess) return BI_GEMM_ERR_CUDA;
   const int64_t units = T * h->Hkv * int64_t(p.max_splits);
-  const unsigned grid = unsigned(std::min<int64_t>(units, h->max_ctas));
   void* args[1] = {&p};
-  if (cudaLaunchKernel(h->kern.fn, dim3(grid), dim3(biattn::kThreads), args, h->smem, st) != cudaSuccess ||
-      cudaLaunchKernel(h->kern.merge, dim3(unsigned(T * h->Hkv)), dim3(biattn::kMergeThreads), args, 0, st) !=
-          cudaSuccess) {
+  void* targs[3] = {&tmk, &tmv, &p};
+  // the attention and merge kernels are launched as programmatic dependents: each may start
+  // while its predecessor runs and waits (griddepcontrol.wait) before it reads what that wrote
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (use_tma) {
+    cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, h->tma_ctas)));
+    cfg.blockDim = dim3(biattn::kTmaThreads);
+    cfg.dynamicSmemBytes = h->tma_smem;
+  } else {
+    cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, h->max_ctas)));
+    cfg.blockDim = dim3(biattn::kThreads);
+    cfg.dynamicSmemBytes = h->smem;
+  }
+  cudaError_t e = cudaLaunchKernelExC(&cfg, use_tma ? h->kern.tma : h->kern.fn, use_tma ? targs : args);
+  if (e == cudaSuccess) {
+    cfg.gridDim = dim3(unsigned(T * h->Hkv));
+    cfg.blockDim = dim3(biattn::kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelExC(&cfg, h->kern.merge, args);
+  }
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return BI_GEMM_ERR_CUDA;
   }
@@ -744,7 +1236,7 @@ BI_GEMM_API int bi_attention_get_device_error(bi_attention_t h, void* stream) {
     cudaGetLastError();
     return BI_GEMM_ERR_CUDA;
   }
-  return BI_GEMM_ERR_INVALID_ARG;
+  return (s & biattn::kErrTimeout) ? BI_GEMM_ERR_TIMEOUT : BI_GEMM_ERR_INVALID_ARG;
 }
 
 BI_GEMM_API int bi_attention_get_config(bi_attention_t h, bi_attention_config* c) {
@@ -754,10 +1246,12 @@ BI_GEMM_API int bi_attention_get_config(bi_attention_t h, bi_attention_config* c
   c->head_dim = h->D;
   c->page_size = h->page_size;
   c->split_size = h->split;
-  c->threads = biattn::kThreads;
+  c->threads = h->tma ? biattn::kTmaThreads : biattn::kThreads;
   c->stage_positions = biattn::kStagePos;
-  c->max_ctas = h->max_ctas;
+  c->max_ctas = h->tma ? h->tma_ctas : h->max_ctas;
   c->num_sms = h->num_sms;
+  c->tma_pages = h->tma ? 1 : 0;
+  c->ring_stages = h->tma ? h->nstage : biattn::kStages;
   return BI_GEMM_OK;
 }
 

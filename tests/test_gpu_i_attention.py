@@ -224,3 +224,38 @@ def test_empty_batch_and_misaligned_pointers():
                               V(zb.data_ptr()), V(zb.data_ptr()), 1, V(z.data_ptr()), 1, 1, 0, V(zb.data_ptr()),
                               V(stream_ptr())) == bg.BI_GEMM_ERR_ALIGNMENT
     attn.close()
+
+
+def test_tma_page_boxes_and_row_copies_give_the_same_bits():
+    """Page sizes 8, 16, 32 and 64 run the kernel whose producer warp loads pages as TMA boxes;
+    other page sizes the kernel whose threads copy rows.  Their arithmetic is the same, so the
+    same requests give the same bits whichever runs, including ragged last stages (lengths that
+    end inside a page and inside a 16-position step) and single-key splits."""
+    Hq, Hkv, D = 32, 8, 128
+    lens = [1, 15, 17, 63, 64, 65, 200, 511, 512, 513, 1000, 2049]
+    outs, flags = {}, {}
+    for page in (8, 16, 32, 64, 12, 1):
+        attn = BiAttention(Hq, Hkv, D, page, split_size=512)
+        flags[page] = attn.config["tma_pages"]
+        outs[page] = decode_batch(lens, Hq, Hkv, D, page, page_seed=page).run(attn)
+        assert attn.device_error() == 0
+        attn.close()
+    assert flags == {8: 1, 16: 1, 32: 1, 64: 1, 12: 0, 1: 0}
+    for page in (16, 32, 64, 12, 1):
+        assert byte_diffs(outs[page], outs[8]) == 0, page
+
+
+@pytest.mark.parametrize("D,G", [(64, 8), (64, 1), (128, 2)])
+def test_tma_page_boxes_other_head_shapes(D, G):
+    """The TMA kernel for other head dimensions and group sizes against the row-copy kernel."""
+    Hkv = 4
+    lens = [3, 64, 129, 777]
+    a = BiAttention(G * Hkv, Hkv, D, 16, split_size=256)
+    b = BiAttention(G * Hkv, Hkv, D, 4, split_size=256)
+    assert a.config["tma_pages"] == 1 and b.config["tma_pages"] == 0
+    oa = decode_batch(lens, G * Hkv, Hkv, D, 16).run(a)
+    ob = decode_batch(lens, G * Hkv, Hkv, D, 4).run(b)
+    assert a.device_error() == 0 and b.device_error() == 0
+    assert byte_diffs(oa, ob) == 0
+    a.close()
+    b.close()
