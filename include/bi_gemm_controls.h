@@ -16,6 +16,7 @@
 
 #include <stdint.h>
 
+#include "bi_attention.h"
 #include "bi_gemm.h"
 
 #ifdef __cplusplus
@@ -66,6 +67,30 @@ int bi_ctl_run_skip_arrival(bi_gemm_t h, const void* x, int64_t M, const void* W
  * fp32 [M, d] device pointers, 16-byte aligned; codes as bi_rmsnorm_run. */
 int bi_ctl_rmsnorm_f32(const void* x, int64_t M, int64_t d, const void* g, float eps, void* y,
                        int32_t mkeyed, void* stream);
+
+/* This library's own copies of bi_attention_create / _run / _get_device_error / _destroy
+ * (include/bi_attention.h, same arguments and codes): a handle made here is used only with
+ * this library's functions. */
+int bi_ctl_attention_create(bi_attention_t* out, int64_t num_q_heads, int64_t num_kv_heads,
+                            int64_t head_dim, int64_t page_size, float scale, int64_t split_size);
+int bi_ctl_attention_run(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,
+                         const int32_t* q_pos, const void* k_cache, const void* v_cache,
+                         int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                         int64_t max_pages, int64_t max_pos, void* o, void* stream);
+int bi_ctl_attention_get_device_error(bi_attention_t h, void* stream);
+int bi_ctl_attention_destroy(bi_attention_t h);
+
+/* Failure injection for the TMA page-box attention kernel (include/bi_attention.h; a handle
+ * whose config has tma_pages = 1, else BI_GEMM_ERR_UNSUPPORTED): bi_attention_run with block 0's
+ * producer never issuing its first load and the ring waits limited to timeout_ns (> 0).  Block
+ * 0's consumer waits expire, the block stops and waits (bounded) for its copies in flight;
+ * bi_attention_get_device_error then reads BI_GEMM_ERR_TIMEOUT and o is undefined.  The handle
+ * stays usable. */
+int bi_ctl_attention_stall(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,
+                           const int32_t* q_pos, const void* k_cache, const void* v_cache,
+                           int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                           int64_t max_pages, int64_t max_pos, void* o, uint64_t timeout_ns,
+                           void* stream);
 
 #ifdef __cplusplus
 }

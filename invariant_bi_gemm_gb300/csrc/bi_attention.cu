@@ -76,6 +76,8 @@ struct Params {
   int32_t Hq, Hkv, page_size, split, max_splits;
   int32_t max_pos;   // the host's bound on q_pos
   int32_t nstage;    // ring depth of the TMA variant
+  int32_t stall_block;   // failure injection (test controls only): this block never issues its
+                         // first load; -1 in the product
   uint64_t timeout_ns;   // limit of its bounded waits
   float c;           // scale * log2(e)
 };
@@ -602,6 +604,7 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
         const int idx0 = sub * ppst;                     // first page of the stage in the unit
         const int cnt = min(ppst, npu - idx0);           // pages of the stage that hold keys
         const uint32_t full = bars + 8 * slot;
+        if (seq == 0 && int(blockIdx.x) == p.stall_block) continue;
         if (lane == 0) ptx::mbar_arrive_expect_tx(full, uint32_t(cnt * TC::HALVES) * box_bytes);
         __syncwarp();
         const int k = idx0 >> 5, l0 = idx0 & 31;         // a stage's pages sit in one register
@@ -1112,10 +1115,14 @@ BI_GEMM_API int bi_attention_workspace_size(bi_attention_t h, int64_t T, int64_t
   return BI_GEMM_OK;
 }
 
-BI_GEMM_API int bi_attention_run(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,
-                                 const int32_t* q_pos, const void* k_cache, const void* v_cache,
-                                 int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
-                                 int64_t max_pages, int64_t max_pos, void* o, void* stream) {
+namespace {
+
+// bi_attention_run with the failure injection of the test controls (stall_block >= 0: that
+// block of the TMA kernel never issues its first load) and the limit of the ring waits.
+int attention_run(bi_attention* h, const void* q, int64_t T, const int32_t* q_seq, const int32_t* q_pos,
+                  const void* k_cache, const void* v_cache, int64_t num_pages, const int32_t* page_table,
+                  int64_t num_seqs, int64_t max_pages, int64_t max_pos, void* o, void* stream, int32_t stall_block,
+                  uint64_t timeout_ns) {
   if (!h || T < 0 || num_pages < 0 || num_seqs < 0 || max_pages < 0 || max_pos < 0) return BI_GEMM_ERR_INVALID_ARG;
   if (T == 0) return BI_GEMM_OK;
   if (T > (int64_t(1) << 24) || max_pos >= (int64_t(1) << 30) ||
@@ -1175,7 +1182,8 @@ BI_GEMM_API int bi_attention_run(bi_attention_t h, const void* q, int64_t T, con
   p.max_pos = int32_t(max_pos);
   p.c = h->scale * 1.4426950408889634f;   // log2(e)
   p.nstage = h->nstage;
-  p.timeout_ns = biattn::kTimeoutNs;
+  p.stall_block = stall_block;
+  p.timeout_ns = timeout_ns;
   // The TMA variant needs the caches' rows addressable by int32 box coordinates (one page past
   // the end included); otherwise, or if a tensor map cannot be encoded, the row-copy kernel
   // runs: both give the same bits.
@@ -1220,6 +1228,16 @@ BI_GEMM_API int bi_attention_run(bi_attention_t h, const void* q, int64_t T, con
     return BI_GEMM_ERR_CUDA;
   }
   return BI_GEMM_OK;
+}
+
+}  // namespace
+
+BI_GEMM_API int bi_attention_run(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,
+                                 const int32_t* q_pos, const void* k_cache, const void* v_cache,
+                                 int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                                 int64_t max_pages, int64_t max_pos, void* o, void* stream) {
+  return attention_run(h, q, T, q_seq, q_pos, k_cache, v_cache, num_pages, page_table, num_seqs, max_pages, max_pos,
+                       o, stream, -1, biattn::kTimeoutNs);
 }
 
 BI_GEMM_API int bi_attention_get_device_error(bi_attention_t h, void* stream) {

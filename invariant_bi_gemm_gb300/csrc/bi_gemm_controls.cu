@@ -14,6 +14,7 @@
 #define BI_GEMM_API extern "C" __attribute__((visibility("hidden")))
 #include "bi_gemm.cu"
 #include "bi_rmsnorm.cu"
+#include "bi_attention.cu"
 
 #include <cuda_bf16.h>
 
@@ -149,4 +150,35 @@ BI_CTL_API int bi_ctl_rmsnorm_f32(const void* x, int64_t M, int64_t d, const voi
   const unsigned grid = unsigned(std::min<int64_t>(M, 1024));
   birms::rmsnorm_kernel<true><<<grid, unsigned(threads), 0, static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? BI_GEMM_OK : BI_GEMM_ERR_CUDA;
+}
+
+// This library's own copies of the attention entry points (the product's are hidden here).
+BI_CTL_API int bi_ctl_attention_create(bi_attention_t* out, int64_t num_q_heads, int64_t num_kv_heads,
+                                       int64_t head_dim, int64_t page_size, float scale, int64_t split_size) {
+  return bi_attention_create(out, num_q_heads, num_kv_heads, head_dim, page_size, scale, split_size);
+}
+
+BI_CTL_API int bi_ctl_attention_run(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,
+                                    const int32_t* q_pos, const void* k_cache, const void* v_cache,
+                                    int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                                    int64_t max_pages, int64_t max_pos, void* o, void* stream) {
+  return bi_attention_run(h, q, T, q_seq, q_pos, k_cache, v_cache, num_pages, page_table, num_seqs, max_pages,
+                          max_pos, o, stream);
+}
+
+BI_CTL_API int bi_ctl_attention_get_device_error(bi_attention_t h, void* stream) {
+  return bi_attention_get_device_error(h, stream);
+}
+
+BI_CTL_API int bi_ctl_attention_destroy(bi_attention_t h) { return bi_attention_destroy(h); }
+
+BI_CTL_API int bi_ctl_attention_stall(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,
+                                      const int32_t* q_pos, const void* k_cache, const void* v_cache,
+                                      int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                                      int64_t max_pages, int64_t max_pos, void* o, uint64_t timeout_ns,
+                                      void* stream) {
+  if (!h) return BI_GEMM_ERR_INVALID_ARG;
+  if (!h->tma || timeout_ns == 0) return BI_GEMM_ERR_UNSUPPORTED;
+  return attention_run(h, q, T, q_seq, q_pos, k_cache, v_cache, num_pages, page_table, num_seqs, max_pages, max_pos, o,
+                       stream, 0, timeout_ns);
 }

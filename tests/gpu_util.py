@@ -92,9 +92,15 @@ class Controls:
         L.bi_ctl_run_stall.argtypes = [P, P, I64, P, P, P, P]
         L.bi_ctl_run_skip_arrival.argtypes = [P, P, I64, P, P, P, P]
         L.bi_ctl_rmsnorm_f32.argtypes = [P, I64, I64, P, ctypes.c_float, P, ctypes.c_int32, P]
+        L.bi_ctl_attention_stall.argtypes = [P, P, I64, P, P, P, P, I64, P, I64, I64, I64, P, ctypes.c_uint64, P]
+        L.bi_ctl_attention_create.argtypes = [ctypes.POINTER(P), I64, I64, I64, I64, ctypes.c_float, I64]
+        L.bi_ctl_attention_run.argtypes = [P, P, I64, P, P, P, P, I64, P, I64, I64, I64, P, P]
+        L.bi_ctl_attention_get_device_error.argtypes = [P, P]
+        L.bi_ctl_attention_destroy.argtypes = [P]
         for n in ("bi_ctl_create", "bi_ctl_destroy", "bi_ctl_get_device_error", "bi_ctl_run",
                   "bi_ctl_msplit_count", "bi_ctl_run_msplit", "bi_ctl_run_smallm_fork", "bi_ctl_run_stall",
-                  "bi_ctl_run_skip_arrival", "bi_ctl_rmsnorm_f32"):
+                  "bi_ctl_run_skip_arrival", "bi_ctl_rmsnorm_f32", "bi_ctl_attention_stall", "bi_ctl_attention_create",
+                  "bi_ctl_attention_run", "bi_ctl_attention_get_device_error", "bi_ctl_attention_destroy"):
             getattr(L, n).restype = I32
         self.L = L
 

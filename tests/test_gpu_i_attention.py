@@ -8,6 +8,8 @@ the negative control the harness must catch (a split size chosen from the batch 
 Workload: q, K, V ~ N(0, 1) in bf16, each request's content from its own stream; physical pages
 handed out by a seeded permutation; the main shape is 32 query heads on 8 KV heads of 128
 (grouped, G = 4) with 16-position pages."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -259,3 +261,41 @@ def test_tma_page_boxes_other_head_shapes(D, G):
     assert byte_diffs(oa, ob) == 0
     a.close()
     b.close()
+
+
+def test_tma_ring_wait_expires_reports_timeout_and_handle_survives():
+    """Failure injection (test controls): block 0's producer never issues its first load, so its
+    consumers' bounded waits on the ring expire after 50 ms; the run reports BI_GEMM_ERR_TIMEOUT
+    through bi_attention_get_device_error, and the next ordinary run on the same handle gives
+    the golden bits.  The handle lives in the controls library (each library has its own CUDA
+    runtime, so a handle is used only with the library that made it)."""
+    from gpu_util import Controls
+    L = Controls().L
+    P = ctypes.c_void_p
+    Hq, Hkv, D = 32, 8, 128
+    bt = decode_batch([700, 1500, 64], Hq, Hkv, D, 16)
+    attn = BiAttention(Hq, Hkv, D, 16)
+    assert attn.config["tma_pages"] == 1
+    golden = bt.run(attn)
+    assert attn.device_error() == 0
+    h = P()
+    assert L.bi_ctl_attention_create(ctypes.byref(h), Hq, Hkv, D, 16, ctypes.c_float(attn.scale), 0) == 0
+    d = {k: torch.from_numpy(getattr(bt, k)).cuda() for k in ("q_seq", "q_pos", "table")}
+    bf = {k: torch.from_numpy(getattr(bt, k).view(np.int16)).cuda().view(torch.bfloat16) for k in ("q", "kc", "vc")}
+    o = torch.empty_like(bf["q"])
+    V = ctypes.c_void_p
+    args = (V(bf["q"].data_ptr()), bf["q"].shape[0], V(d["q_seq"].data_ptr()), V(d["q_pos"].data_ptr()),
+            V(bf["kc"].data_ptr()), V(bf["vc"].data_ptr()), bf["kc"].shape[0], V(d["table"].data_ptr()),
+            d["table"].shape[0], d["table"].shape[1], bt.max_pos, V(o.data_ptr()))
+    bits = lambda: o.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert L.bi_ctl_attention_run(h, *args, V(stream_ptr())) == 0
+    assert L.bi_ctl_attention_get_device_error(h, V(stream_ptr())) == 0
+    assert np.array_equal(bits(), golden)
+    o.zero_()
+    assert L.bi_ctl_attention_stall(h, *args, 50_000_000, V(stream_ptr())) == 0
+    assert L.bi_ctl_attention_get_device_error(h, V(stream_ptr())) == bg.BI_GEMM_ERR_TIMEOUT
+    assert L.bi_ctl_attention_run(h, *args, V(stream_ptr())) == 0
+    assert L.bi_ctl_attention_get_device_error(h, V(stream_ptr())) == 0
+    assert np.array_equal(bits(), golden)
+    L.bi_ctl_attention_destroy(h)
+    attn.close()
