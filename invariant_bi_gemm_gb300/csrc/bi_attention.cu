@@ -482,9 +482,16 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
 // the consumers its query rows), so that no dependent load stalls the stream at a unit change.
 // Every wait on the ring is bounded: past the limit the block sets kErrTimeout, stops issuing,
 // waits (bounded) for the copies it has in flight, and leaves.
-constexpr int kConsumers = 4;                 // consumer warps: attn_kernel's layout
-constexpr int kTmaThreads = 32 + kThreads;    // producer warp + consumers
-constexpr int kTmaBlocksPerSm = 3;            // the ring depth is sized for three blocks per SM
+// Consumer warps per block: CW = 4 (attn_kernel's layout) or 8 (head dimension 128 only).  With
+// 8 the positions of a stage and the dimensions of the output are spread over twice the warps;
+// every score and every output element still goes through the same instructions in the same
+// order, and the softmax reductions run on the first 128 consumer threads exactly as in
+// attn_kernel, so the bits do not change.  Four warps at three blocks per SM stream faster than
+// eight at two, so 4 is the choice.
+template <int D>
+constexpr int tma_consumer_warps() { return 4; }
+constexpr int tma_threads(int cw) { return 32 + 32 * cw; }
+constexpr int tma_blocks_per_sm(int cw) { return cw == 8 ? 2 : 3; }   // the ring is sized for these
 constexpr int kTmaMaxStages = 8;
 constexpr uint32_t kErrTimeout = 8u;          // a bounded wait on the ring expired
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -492,10 +499,18 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 template <int D, int G>
 struct TmaCfg {
   using C = Cfg<D, G>;
+  static constexpr int CW = tma_consumer_warps<D>();
+  static constexpr int CT = 32 * CW;                   // consumer threads
+  static constexpr int THREADS = tma_threads(CW);
+  static constexpr int BLOCKS_PER_SM = tma_blocks_per_sm(CW);
+  static constexpr int NT1 = kStagePos / CW / 8;       // score n tiles (8 positions) per warp
+  static constexpr int DW = D / CW;                    // output dimensions per warp
+  static constexpr int NT2 = DW / 8;                   // n tiles per warp in the value MMA
+  static_assert(NT1 >= 1 && NT2 % 2 == 0 && CW >= 4, "consumer warp layout");
   static constexpr int HALVES = D / 64;                // 128-byte column halves of a row
   static constexpr int HALF_BYTES = kStagePos * 128;   // one half of a stage: 64 rows of 128 B
   static constexpr int STAGE_BYTES = HALVES * HALF_BYTES;
-  static constexpr int QW = (G * D / 2 + kThreads - 1) / kThreads;   // query words per consumer
+  static constexpr int QW = (G * D / 2 + CT - 1) / CT;   // query words per consumer
   // 1024-byte alignment slack | ring [nstage] | full, empty barriers [nstage] each | scores
   // [G][stride] | per-warp maxima, sums [G][4] each | maximum, sum [G] each | query rows [G][QS]
   __host__ __device__ static size_t fixed_bytes(int split) {
@@ -521,7 +536,7 @@ __device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, const P
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
+__global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PER_SM)
     attn_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Params p) {
   using C = Cfg<D, G>;
   using TC = TmaCfg<D, G>;
@@ -544,7 +559,7 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
     s_abort = 0u;
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(bars + 8 * s, 1);
-      ptx::mbar_init(bars + 8 * (NS + s), kConsumers);
+      ptx::mbar_init(bars + 8 * (NS + s), TC::CW);
     }
     ptx::fence_barrier_init();
   }
@@ -647,7 +662,8 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
   const int ctid = tid - 32, cw = warp - 1;
   const int gq = lane >> 2, tq = lane & 3;
   const bool row_ok = gq < G;
-  const int dbase = cw * C::DW;
+  const int dbase = cw * TC::DW;
+  constexpr int CT = TC::CT;
   // 16-byte chunk c of staged row r (the boxes' 128-byte swizzle: two column halves of 64 rows)
   auto chunk_addr = [&](uint32_t stage, int r, int c) {
     return stage + uint32_t((c >> 3) * TC::HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4));
@@ -656,7 +672,7 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
     const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q + (w.t * p.Hq + int64_t(w.kh) * G) * D);
 #pragma unroll
     for (int k = 0; k < TC::QW; ++k) {
-      const int i = ctid + k * kThreads;
+      const int i = ctid + k * CT;
       qr[k] = i < G * D / 2 ? src[i] : 0u;
     }
   };
@@ -671,11 +687,11 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
       uint32_t* dst = reinterpret_cast<uint32_t*>(qsm);
 #pragma unroll
       for (int k = 0; k < TC::QW; ++k) {
-        const int i = ctid + k * kThreads;
+        const int i = ctid + k * CT;
         if (i < G * D / 2) dst[(i / (D / 2)) * (C::QS / 2) + i % (D / 2)] = qr[k];
       }
     }
-    ptx::named_bar_sync1<kThreads>();
+    ptx::named_bar_sync1<CT>();
     // this thread's query A fragments for every k step, held for the unit:
     // qa[k][0] = q[gq][16k + 2tq, +1], qa[k][1] = q[gq][16k + 8 + 2tq, +1] (zero past the G heads)
     uint32_t qa[C::KSTEPS][2];
@@ -692,9 +708,9 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
     int4 nrec = make_int4(0, 0, 0, 0);
     Unit nxt = cur;
     const int nload = 2 * cur.nsub;
-    float acc[C::NT2][4];
+    float acc[TC::NT2][4];
 #pragma unroll
-    for (int n = 0; n < C::NT2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+    for (int n = 0; n < TC::NT2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
     for (int i = 0; i < nload; ++i, ++seq) {
       if (i == 0 && has_next) nrec = p.urec[un];
       if (i == 1 && has_next) {
@@ -707,11 +723,11 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
       const uint32_t stage = sbase + uint32_t(slot * TC::STAGE_BYTES);
       if (i < cur.nsub) {
         if (ok) {
-          const int pos0 = i * kStagePos + cw * (kStagePos / 4);
+          const int pos0 = i * kStagePos + cw * (kStagePos / TC::CW);
 #pragma unroll
-          for (int nt = 0; nt < C::NT1; ++nt) {
+          for (int nt = 0; nt < TC::NT1; ++nt) {
             float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const int prow = cw * (kStagePos / 4) + nt * 8 + (lane & 7);
+            const int prow = cw * (kStagePos / TC::CW) + nt * 8 + (lane & 7);
 #pragma unroll
             for (int kp = 0; kp < C::KSTEPS / 2; ++kp) {
               uint32_t b[4];
@@ -727,31 +743,37 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
           }
         }
         if (i == cur.nsub - 1) {
-          ptx::named_bar_sync1<kThreads>();
+          // the split's maximum, weights and sum: attn_kernel's 128-thread tree, on consumer
+          // warps 0..3 (the others wait at the barriers)
+          ptx::named_bar_sync1<CT>();
+          if (cw < 4) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float m = -INFINITY;
-            for (int jj = ctid; jj < cur.valid; jj += kThreads) m = fmaxf(m, sc[g * SCS + jj]);
+            for (int g = 0; g < G; ++g) {
+              float m = -INFINITY;
+              for (int jj = ctid; jj < cur.valid; jj += kThreads) m = fmaxf(m, sc[g * SCS + jj]);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-            if (lane == 0) red[g * 4 + cw] = m;
-          }
-          ptx::named_bar_sync1<kThreads>();
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float m = fmaxf(fmaxf(red[g * 4 + 0], red[g * 4 + 1]), fmaxf(red[g * 4 + 2], red[g * 4 + 3]));
-            float ls = 0.0f;
-            for (int jj = ctid; jj < cur.valid; jj += kThreads) {
-              const float w = exp2f(__fsub_rn(sc[g * SCS + jj], m));
-              sc[g * SCS + jj] = w;
-              ls = __fadd_rn(ls, w);
+              for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+              if (lane == 0) red[g * 4 + cw] = m;
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xFFFFFFFFu, ls, o));
-            if (ctid == 0) hm[g] = m;
-            if (lane == 0) redl[g * 4 + cw] = ls;
           }
-          ptx::named_bar_sync1<kThreads>();
+          ptx::named_bar_sync1<CT>();
+          if (cw < 4) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float m = fmaxf(fmaxf(red[g * 4 + 0], red[g * 4 + 1]), fmaxf(red[g * 4 + 2], red[g * 4 + 3]));
+              float ls = 0.0f;
+              for (int jj = ctid; jj < cur.valid; jj += kThreads) {
+                const float w = exp2f(__fsub_rn(sc[g * SCS + jj], m));
+                sc[g * SCS + jj] = w;
+                ls = __fadd_rn(ls, w);
+              }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xFFFFFFFFu, ls, o));
+              if (ctid == 0) hm[g] = m;
+              if (lane == 0) redl[g * 4 + cw] = ls;
+            }
+          }
+          ptx::named_bar_sync1<CT>();
           if (ctid < G)
             hl[ctid] = __fadd_rn(__fadd_rn(__fadd_rn(redl[ctid * 4 + 0], redl[ctid * 4 + 1]), redl[ctid * 4 + 2]),
                                  redl[ctid * 4 + 3]);
@@ -765,11 +787,11 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
           // zero weights, as the zero-filled rows of attn_kernel do
           if (ok) {
             const int r0 = rows, nr = ((rows + 15) & ~15) - rows;
-            for (int e = ctid; e < nr * (D / 8); e += kThreads)
+            for (int e = ctid; e < nr * (D / 8); e += CT)
               ptx::st_shared_v4(chunk_addr(stage, r0 + e / (D / 8), e % (D / 8)), 0u, 0u, 0u, 0u);
             ptx::fence_proxy_async_smem();   // ordered before the slot's next TMA write
           }
-          ptx::named_bar_sync1<kThreads>();
+          ptx::named_bar_sync1<CT>();
         }
         if (ok) {
           for (int k0 = 0; k0 < rows; k0 += 16) {
@@ -791,7 +813,7 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
               al[h2] = pack_bf16x2(__fsub_rn(x0, h0), __fsub_rn(x1, h1));
             }
 #pragma unroll
-            for (int np = 0; np < C::NT2 / 2; ++np) {
+            for (int np = 0; np < TC::NT2 / 2; ++np) {
               uint32_t b[4];
               const int prow = k0 + ((lane >> 3) & 1) * 8 + (lane & 7);
               ldsm_x4_trans(chunk_addr(stage, prow, (dbase + 16 * np) / 8 + (lane >> 4)), b);
@@ -807,14 +829,14 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
       if (lane == 0) ptx::mbar_arrive(bars + 8 * (NS + slot));   // this warp is done with the slot
     }
 
-    ptx::named_bar_sync1<kThreads>();   // hl is written
+    ptx::named_bar_sync1<CT>();   // hl is written
     if (ok) {
       const int64_t orow = (cur.t * p.Hq + int64_t(cur.kh) * G + gq) * D;
       if (cur.nsplit == 1) {
         if (row_ok) {
           const float l = hl[gq];
 #pragma unroll
-          for (int n = 0; n < C::NT2; ++n)
+          for (int n = 0; n < TC::NT2; ++n)
             *reinterpret_cast<uint32_t*>(p.o + orow + dbase + 8 * n + 2 * tq) =
                 pack_bf16x2(__fdiv_rn(acc[n][0], l), __fdiv_rn(acc[n][1], l));
         }
@@ -822,7 +844,7 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
         const int64_t slot = (cur.t * p.Hkv + cur.kh) * int64_t(p.max_splits) + cur.s;
         if (row_ok) {
 #pragma unroll
-          for (int n = 0; n < C::NT2; ++n)
+          for (int n = 0; n < TC::NT2; ++n)
             *reinterpret_cast<float2*>(p.part + (slot * G + gq) * D + dbase + 8 * n + 2 * tq) =
                 make_float2(acc[n][0], acc[n][1]);
         }
@@ -834,7 +856,7 @@ __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSm)
     }
     // the scores, per-head values and query rows are reused by the next unit; every consumer
     // warp takes the same decision to go on
-    if (ptx::named_bar_or1<kThreads>(!ok) || !has_next) break;
+    if (ptx::named_bar_or1<CT>(!ok) || !has_next) break;
     cur = nxt;
     u = un;
   }
@@ -915,7 +937,7 @@ struct KernelInfo {
   const void* merge = nullptr;
   size_t (*smem)(int) = nullptr;
   size_t (*tma_fixed)(int) = nullptr;   // TMA variant: shared memory besides the ring
-  int tma_stage_bytes = 0;
+  int tma_stage_bytes = 0, tma_threads = 0, tma_blocks_per_sm = 0;
 };
 
 template <int D, int G>
@@ -925,6 +947,8 @@ KernelInfo info() {
   k.tma = reinterpret_cast<const void*>(&attn_tma_kernel<D, G>);
   k.tma_fixed = &TmaCfg<D, G>::fixed_bytes;
   k.tma_stage_bytes = TmaCfg<D, G>::STAGE_BYTES;
+  k.tma_threads = TmaCfg<D, G>::THREADS;
+  k.tma_blocks_per_sm = TmaCfg<D, G>::BLOCKS_PER_SM;
   k.merge = reinterpret_cast<const void*>(&merge_kernel<D, G>);
   k.smem = &Cfg<D, G>::smem_bytes;
   return k;
@@ -1050,7 +1074,7 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
     cudaGetLastError();
     return BI_GEMM_ERR_CUDA;
   }
-  // TMA variant: the deepest ring (up to 8 stages) with which kTmaBlocksPerSm blocks fit on an SM
+  // TMA variant: the deepest ring (up to 8 stages) with which its blocks per SM fit
   bool tma = false;
   int nstage = 0, tma_per_sm = 0;
   size_t tma_smem = 0;
@@ -1064,7 +1088,7 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
       cudaGetLastError();
       return BI_GEMM_ERR_CUDA;
     }
-    const int64_t budget = int64_t(sm_bytes) / biattn::kTmaBlocksPerSm - reserved - int64_t(fa.sharedSizeBytes) -
+    const int64_t budget = int64_t(sm_bytes) / k.tma_blocks_per_sm - reserved - int64_t(fa.sharedSizeBytes) -
                            int64_t(k.tma_fixed(int(split)));
     nstage = int(std::min<int64_t>(biattn::kTmaMaxStages, budget / (k.tma_stage_bytes + 16)));
     if (nstage >= 2 && biattn::encode_fn()) {
@@ -1072,7 +1096,7 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
       // per kernel, shared by every handle of the head shape: the most a block may have
       if (cudaFuncSetAttribute(k.tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                optin - int(fa.sharedSizeBytes)) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&tma_per_sm, k.tma, biattn::kTmaThreads, tma_smem) !=
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&tma_per_sm, k.tma, k.tma_threads, tma_smem) !=
               cudaSuccess) {
         cudaGetLastError();
         return BI_GEMM_ERR_CUDA;
@@ -1209,7 +1233,7 @@ int attention_run(bi_attention* h, const void* q, int64_t T, const int32_t* q_se
   cfg.numAttrs = 1;
   if (use_tma) {
     cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, h->tma_ctas)));
-    cfg.blockDim = dim3(biattn::kTmaThreads);
+    cfg.blockDim = dim3(h->kern.tma_threads);
     cfg.dynamicSmemBytes = h->tma_smem;
   } else {
     cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, h->max_ctas)));
@@ -1264,7 +1288,7 @@ BI_GEMM_API int bi_attention_get_config(bi_attention_t h, bi_attention_config* c
   c->head_dim = h->D;
   c->page_size = h->page_size;
   c->split_size = h->split;
-  c->threads = h->tma ? biattn::kTmaThreads : biattn::kThreads;
+  c->threads = h->tma ? h->kern.tma_threads : biattn::kThreads;
   c->stage_positions = biattn::kStagePos;
   c->max_ctas = h->tma ? h->tma_ctas : h->max_ctas;
   c->num_sms = h->num_sms;
