@@ -641,6 +641,9 @@ def measure_attention(dev, peaks):
     return {"shape": "decode: q[B,32,128] over a paged bf16 KV cache [pages,16,8,128], one token per request at "
                      "position context-1, split size 512 positions",
             "grid_bound": cfg["max_ctas"], "rows": rows, "device_error": err,
+            "kernel": ("TMA page boxes: a producer warp and four consumer warps per block, "
+                       f"{cfg['ring_stages']}-stage ring" if cfg["tma_pages"] else
+                       f"cp.async row copies, {cfg['ring_stages']}-stage ring") + f", {cfg['threads']} threads",
             "bytes": "K and V of every request once (2 x B x context x 8 x 128 x 2) + q and o",
             "note": "graph-timed; pages shuffled over the cache; three kernels per call (plan, attention, merge)"}
 
