@@ -513,10 +513,10 @@ struct TmaCfg {
   static constexpr int QW = (G * D / 2 + CT - 1) / CT;   // query words per consumer
   // 1024-byte alignment slack | ring [nstage] | full, empty barriers [nstage] each | scores
   // [G][stride] | per-warp maxima, sums [G][4] each | maximum, sum [G] each | query rows [G][QS]
-  __host__ __device__ static size_t fixed_bytes(int split) {
+  // (the host adds nstage x (STAGE_BYTES + 16) for the ring and its barriers)
+  static size_t fixed_bytes(int split) {
     return 1024 + sizeof(float) * (size_t(G) * C::sc_stride(split) + G * 10) + sizeof(uint16_t) * G * C::QS;
   }
-  static size_t smem_bytes(int split, int nstage) { return fixed_bytes(split) + size_t(nstage) * (STAGE_BYTES + 16); }
 };
 
 // Bounded wait for a phase of a ring barrier: false (status set, block aborted) past the time
