@@ -195,3 +195,38 @@ def test_product_path_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "bi_oracle" not in src and "from oracle" not in src and "import oracle" not in src
+
+
+def _structs(header):
+    """{typedef name: [(C type, field), ...]} of the plain structs a header declares."""
+    src = open(os.path.join(ROOT, "include", header)).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for body, name in re.findall(r"typedef struct\s*\{(.*?)\}\s*(\w+)\s*;", src, flags=re.S):
+        fields = []
+        for decl in body.split(";"):
+            decl = decl.strip()
+            if not decl:
+                continue
+            m = re.match(r"((?:const\s+)?\w+\s*\**)\s*(.+)", decl)
+            ctype, names = m.group(1).replace(" ", ""), m.group(2)
+            fields += [(ctype, n.strip()) for n in names.split(",")]
+        out[name] = fields
+    return out
+
+
+@pytest.mark.parametrize("header,name,cls", [
+    ("bi_gemm.h", "bi_gemm_config", "bi_gemm_config"),
+    ("bi_gemm.h", "bi_gemm_options", "bi_gemm_options"),
+    ("bi_rmsnorm.h", "bi_rmsnorm_config", "bi_rmsnorm_config"),
+    ("bi_attention.h", "bi_attention_config", "bi_attention_config"),
+    ("bi_prenorm.h", "bi_prenorm_config", "bi_prenorm_config"),
+])
+def test_binding_structs_match_the_headers(header, name, cls):
+    """The ctypes structures of the binding list the header's fields in the header's order with
+    the header's widths, so a field added on one side only is caught without a GPU."""
+    width = {"int32_t": ctypes.c_int32, "uint64_t": ctypes.c_uint64, "int64_t": ctypes.c_int64}
+    fields = _structs(header)[name]
+    py = getattr(bg, cls)._fields_
+    assert [n for _, n in fields] == [n for n, _ in py]
+    assert [width[t] for t, _ in fields] == [t for _, t in py]
