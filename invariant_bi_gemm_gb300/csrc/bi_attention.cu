@@ -50,6 +50,38 @@ namespace biattn {
 
 namespace ptx = bigemm::ptx;
 
+// 3-D tiled bulk tensor load global -> shared (c0 innermost), completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0,
+                                            int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+// Barrier 1 for kThreadsInBarrier threads (whole warps): synchronises a subset of the block.
+template <int kThreadsInBarrier>
+__device__ __forceinline__ void named_bar_sync1() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreadsInBarrier) : "memory");
+}
+
+// Barrier 1 for kThreadsInBarrier threads with an OR over their predicates: every participant
+// gets the same answer.
+template <int kThreadsInBarrier>
+__device__ __forceinline__ bool named_bar_or1(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(pred)), "n"(kThreadsInBarrier)
+      : "memory");
+  return r != 0;
+}
+
 constexpr int kThreads = 128;        // threads per block (four warps)
 constexpr int kStagePos = 64;        // positions per staged key / value tile
 constexpr int kMergeThreads = 1024;  // merge block: four threads per output pair
@@ -631,7 +663,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
           const uint32_t dst = sbase + uint32_t(slot * TC::STAGE_BYTES) + uint32_t(lane - l0) * box_bytes;
 #pragma unroll
           for (int hh = 0; hh < TC::HALVES; ++hh)
-            ptx::tma_load_3d(dst + hh * TC::HALF_BYTES, isv ? &tmv : &tmk, full, hh * 64, cur.kh, row);
+            tma_load_3d(dst + hh * TC::HALF_BYTES, isv ? &tmv : &tmk, full, hh * 64, cur.kh, row);
         }
       }
       if (stop || !has_next) break;
@@ -691,7 +723,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
         if (i < G * D / 2) dst[(i / (D / 2)) * (C::QS / 2) + i % (D / 2)] = qr[k];
       }
     }
-    ptx::named_bar_sync1<CT>();
+    named_bar_sync1<CT>();
     // this thread's query A fragments for every k step, held for the unit:
     // qa[k][0] = q[gq][16k + 2tq, +1], qa[k][1] = q[gq][16k + 8 + 2tq, +1] (zero past the G heads)
     uint32_t qa[C::KSTEPS][2];
@@ -745,7 +777,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
         if (i == cur.nsub - 1) {
           // the split's maximum, weights and sum: attn_kernel's 128-thread tree, on consumer
           // warps 0..3 (the others wait at the barriers)
-          ptx::named_bar_sync1<CT>();
+          named_bar_sync1<CT>();
           if (cw < 4) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -756,7 +788,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
               if (lane == 0) red[g * 4 + cw] = m;
             }
           }
-          ptx::named_bar_sync1<CT>();
+          named_bar_sync1<CT>();
           if (cw < 4) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -773,7 +805,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
               if (lane == 0) redl[g * 4 + cw] = ls;
             }
           }
-          ptx::named_bar_sync1<CT>();
+          named_bar_sync1<CT>();
           if (ctid < G)
             hl[ctid] = __fadd_rn(__fadd_rn(__fadd_rn(redl[ctid * 4 + 0], redl[ctid * 4 + 1]), redl[ctid * 4 + 2]),
                                  redl[ctid * 4 + 3]);
@@ -791,7 +823,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
               ptx::st_shared_v4(chunk_addr(stage, r0 + e / (D / 8), e % (D / 8)), 0u, 0u, 0u, 0u);
             ptx::fence_proxy_async_smem();   // ordered before the slot's next TMA write
           }
-          ptx::named_bar_sync1<CT>();
+          named_bar_sync1<CT>();
         }
         if (ok) {
           for (int k0 = 0; k0 < rows; k0 += 16) {
@@ -829,7 +861,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
       if (lane == 0) ptx::mbar_arrive(bars + 8 * (NS + slot));   // this warp is done with the slot
     }
 
-    ptx::named_bar_sync1<CT>();   // hl is written
+    named_bar_sync1<CT>();   // hl is written
     if (ok) {
       const int64_t orow = (cur.t * p.Hq + int64_t(cur.kh) * G + gq) * D;
       if (cur.nsplit == 1) {
@@ -856,7 +888,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
     }
     // the scores, per-head values and query rows are reused by the next unit; every consumer
     // warp takes the same decision to go on
-    if (ptx::named_bar_or1<CT>(!ok) || !has_next) break;
+    if (named_bar_or1<CT>(!ok) || !has_next) break;
     cur = nxt;
     u = un;
   }

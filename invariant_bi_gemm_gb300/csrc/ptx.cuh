@@ -86,38 +86,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// 3-D tiled bulk tensor load global -> shared (c0 innermost), completion counted in bytes on `bar`.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0,
-                                            int32_t c1, int32_t c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-
-// Barrier 1 for kThreadsInBarrier threads (whole warps): synchronises a subset of the block.
-template <int kThreadsInBarrier>
-__device__ __forceinline__ void named_bar_sync1() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kThreadsInBarrier) : "memory");
-}
-
-// Barrier 1 for kThreadsInBarrier threads with an OR over their predicates: every participant
-// gets the same answer.
-template <int kThreadsInBarrier>
-__device__ __forceinline__ bool named_bar_or1(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "barrier.cta.red.or.pred q, 1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(uint32_t(pred)), "n"(kThreadsInBarrier)
-      : "memory");
-  return r != 0;
-}
-
 // 2-D tiled bulk tensor store shared -> global (rows / columns outside the tensor are not
 // written), tracked in this thread's bulk-async group.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t c0,
