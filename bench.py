@@ -36,7 +36,13 @@ METRIC = "TFLOP/s & % roofline vs M (1-8192), 0 byte-diff batch invariance, 1 GB
 WORKLOAD = "LLM projection sweep: bf16 x[M,4096]·W[4096,14336], fp32 accumulate, bf16 out, M in 1..8192 (19 values)"
 KERNEL_SOURCES = ["invariant_bi_gemm_gb300/csrc/bi_gemm_kernel.cuh", "invariant_bi_gemm_gb300/csrc/ptx.cuh",
                   "invariant_bi_gemm_gb300/csrc/bi_gemm.cu"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_bf16_gemm_llm_sweep.md")
+# The GEMM handle of the sweep is created with BI_GEMM_FLAG_STATIC_W: W is never written while
+# the sweep runs, so each launch may start loading W before the previous launch has finished.
+STATIC_W = True
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of each launch of the sweep, from one
+# ncu capture of `python bench.py --steps 1 --warmup 3 --no-paths --no-cpu` (the command and the
+# figures are in profiles/ncu_bf16_gemm_llm_sweep.md), for the kernel sources of the given hash.
+TRAFFIC = {"source_sha256_16": None, "bytes_per_launch": {}}
 
 
 def flops(M, K=K_DIM, N=N_DIM):
@@ -71,25 +77,12 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """Per-launch DRAM bytes of the sweep's GEMM kernel from the committed ncu summary, or None
-    when the kernel sources changed since it was captured."""
-    try:
-        txt = open(TRAFFIC_FILE).read()
-    except OSError:
+def recorded_traffic(M):
+    """DRAM bytes (read + written) of the sweep's launch at M from the ncu capture recorded in
+    TRAFFIC, or None when the kernel sources changed since that capture."""
+    if TRAFFIC.get("source_sha256_16") != kernel_hash():
         return None
-    vals = {}
-    for line in txt.splitlines():
-        line = line.strip().strip("`")
-        if ":" in line and line.split(":", 1)[0].strip() in ("source_sha256_16", "traffic_bytes_per_launch"):
-            k, v = line.split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("source_sha256_16") != kernel_hash():
-        return None
-    try:
-        return float(vals["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    return TRAFFIC["bytes_per_launch"].get(M)
 
 
 # ------------------------------------------------------------------ clocks
@@ -186,57 +179,96 @@ def max_over_ranks(v, world):
 
 # ------------------------------------------------------------------ CPU oracle baseline
 
-def oracle_sample(budget_s: float, min_cols: int = 64):
-    """Time the CPU oracle on rows of the sweep's x against W until `budget_s` passes.
+def oracle_sample(budget_s: float, threads: int = 1):
+    """Time the CPU oracle on rows of the sweep's x against the full W for about `budget_s`
+    seconds of wall time.  With threads > 1 the rows are spread over that many threads, each
+    calling the unchanged single-threaded oracle on one row at a time (the C call releases the
+    interpreter lock; rows are independent, so the results are those of one thread).
 
     Returns (flops_done, seconds, description)."""
-    import numpy as np
-    import inputgen as ig
-    import oracle
-    W = ig.normal_bf16(ig.SEED_W, K_DIM, N_DIM, std=0.02)
-    x = ig.normal_bf16(ig.SEED_X, 64, K_DIM)
-    done_rows, t_total = 0, 0.0
-    while t_total < budget_s and done_rows < 64:
-        t0 = time.perf_counter()
-        oracle.gemm_bf16(x[done_rows:done_rows + 1], W, "bf16")
-        t_total += time.perf_counter() - t0
-        done_rows += 1
-    desc = (f"{done_rows} rows of x[8192,4096] times the full W[4096,14336] (all 14336 outputs per row), "
-            f"plain C oracle, fp64, one thread")
-    return flops(done_rows), t_total, desc
+    import threading
+    from concurrent.futures import ThreadPoolExecutor
 
-
-def run_reference(args, rank, world):
-    if rank != 0:
-        return
-    import numpy as np
     import inputgen as ig
     import oracle
     oracle.lib()
     W = ig.normal_bf16(ig.SEED_W, K_DIM, N_DIM, std=0.02)
-    x = ig.normal_bf16(ig.SEED_X, 1, K_DIM)
+    rows = min(8192, 16 * threads)
+    x = ig.normal_bf16(ig.SEED_X, rows, K_DIM)
+    lock = threading.Lock()
+    state = {"next": 0, "done": 0}
+    t0 = time.perf_counter()
+
+    def worker():
+        while time.perf_counter() - t0 < budget_s:
+            with lock:
+                r = state["next"]
+                if r >= rows:
+                    return
+                state["next"] = r + 1
+            oracle.gemm_bf16(x[r:r + 1], W, "bf16")
+            with lock:
+                state["done"] += 1
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for f in [ex.submit(worker) for _ in range(threads)]:
+            f.result()
+    dt = time.perf_counter() - t0
+    done = state["done"]
+    desc = (f"{done} rows of x[8192,4096] times the full W[4096,14336] (all 14336 outputs per row), "
+            f"plain C oracle, fp64, {threads} thread{'s' if threads > 1 else ''} (one row per call)")
+    return flops(done), dt, desc
+
+
+def roof_time(M, peaks, K=K_DIM, N=N_DIM):
+    """Seconds of one launch at its roofline: max(FLOP / tensor peak, algorithmic bytes / HBM)."""
+    return max(flops(M, K, N) / (peaks["bf16_tflops"] * 1e12), algo_bytes(M, K, N) / (peaks["hbm_gbs"] * 1e9))
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, on all host cores (one thread per core,
+    each running the single-threaded oracle on its own row), on a bounded sample of the same
+    workload per step."""
+    if rank != 0:
+        return
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+    import inputgen as ig
+    import oracle
+    oracle.lib()
+    cores = os.cpu_count() or 1
+    W = ig.normal_bf16(ig.SEED_W, K_DIM, N_DIM, std=0.02)
+    x = ig.normal_bf16(ig.SEED_X, cores, K_DIM)
     # calibrate one full row, then size each step's sample so the whole run stays near 2 minutes
     t0 = time.perf_counter()
-    oracle.gemm_bf16(x, W, "bf16")
+    oracle.gemm_bf16(x[:1], W, "bf16")
     t_row = time.perf_counter() - t0
     per_step = 120.0 / max(1, args.steps + args.warmup)
     cols = int(max(64, min(N_DIM, N_DIM * per_step / max(t_row, 1e-6))) // 64 * 64)
     Wc = np.ascontiguousarray(W[:, :cols])
-    for _ in range(args.warmup):
-        oracle.gemm_bf16(x, Wc, "bf16")
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.gemm_bf16(x, Wc, "bf16")
-    dt = time.perf_counter() - t0
-    fl = flops(1, K_DIM, cols) * args.steps
+
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        def step():
+            for f in [ex.submit(oracle.gemm_bf16, x[r:r + 1], Wc, "bf16") for r in range(cores)]:
+                f.result()
+
+        for _ in range(args.warmup):
+            step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step()
+        dt = time.perf_counter() - t0
+    fl = flops(cores, K_DIM, cols) * args.steps
     v = fl / dt / 1e12
-    sample = f"per step: 1 row of x times W[:, :{cols}] of the LLM projection (K=4096), plain C oracle, fp64, one thread"
+    sample = (f"per step: {cores} rows of x (one per thread) times W[:, :{cols}] of the LLM projection (K=4096), "
+              f"plain C oracle, fp64, {cores} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_obj(world),
-        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -270,7 +302,7 @@ def run_ours(args, rank, world, local):
     Ws = [W0] + [W0.clone() for _ in range(N_SETS - 1)]
     Xs = [X0] + [X0.clone() for _ in range(N_SETS - 1)]
     Y = torch.empty((M_SWEEP[-1], N_DIM), dtype=torch.bfloat16, device=dev)
-    g = BiGemm(K_DIM, N_DIM, "bf16")
+    g = BiGemm(K_DIM, N_DIM, "bf16", static_w=STATIC_W)
     stream = torch.cuda.current_stream(dev)
     nM = len(M_SWEEP)
 
@@ -351,36 +383,60 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     eager_ms = e0.elapsed_time(e1) / n_eager
 
+    cublas = measure_cublas_context(Xs, Ws, g, stream)
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     sweep = []
     for M in M_SWEEP:
         t = per_m[M] / 1e3
         fl, by = flops(M), algo_bytes(M)
-        t_roof = max(fl / (peaks["bf16_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9))
+        t_roof = roof_time(M, peaks)
         tw = per_m_warm[M] / 1e3
-        sweep.append({"M": M, "us": round(t * 1e6, 2), "tflops": round(fl / t / 1e12, 2),
-                      "gbs": round(by / t / 1e9, 1), "bound": "hbm" if fl / by < ridge else "tensor",
-                      "frac": round(t_roof / t, 3), "us_warm_l2": round(tw * 1e6, 2),
-                      "tflops_warm_l2": round(fl / tw / 1e12, 2)})
+        row = {"M": M, "us": round(t * 1e6, 2), "tflops": round(fl / t / 1e12, 2),
+               "gbs": round(by / t / 1e9, 1), "bound": "hbm" if fl / by < ridge else "tensor",
+               "frac": round(t_roof / t, 3), "us_warm_l2": round(tw * 1e6, 2),
+               "tflops_warm_l2": round(fl / tw / 1e12, 2), "algorithmic_bytes": int(by)}
+        tr = recorded_traffic(M)
+        row["dram_bytes"] = tr
+        row["dram_over_algorithmic"] = round(tr / by, 3) if tr else None
+        row.update(cublas.get(M, {}))
+        sweep.append(row)
 
-    achieved = step_flops / (kernel_ms_total / 1e3) / 1e12
-    traffic = recorded_traffic()
-    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
-                "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
+    # Roofline of the timed region (the whole sweep): the step's time at the roofline is the sum,
+    # over its launches, of max(FLOP / tensor peak, bytes / HBM bandwidth); `peak` is the FLOP rate
+    # of a step that ran every launch at its roofline, so frac = achieved / peak = that sum / the
+    # measured step time.
+    t_step = elapsed_ms / args.steps / 1e3
+    t_roof_step = sum(roof_time(M, peaks) for M in M_SWEEP)
+    achieved = step_flops / t_step / 1e12
+    peak_step = step_flops / t_roof_step / 1e12
+    traffic = [recorded_traffic(M) for M in M_SWEEP]
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak_step, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak_step, 4),
+                "traffic": int(sum(traffic)) if all(traffic) else None,
+                "algorithmic_bytes": int(sum(algo_bytes(M) for M in M_SWEEP)),
+                "per": "one step (19 launches of the sweep); traffic is DRAM read + write bytes of those launches "
+                       "from one ncu capture (null when the kernel changed since)",
+                "peak_definition": "sum over the step's launches of max(2MKN / tensor peak, bytes / HBM bandwidth); "
+                                   "frac = that time / ms_per_step",
+                "peak_tensor_tflops": peaks["bf16_tflops"], "peak_hbm_gbs": peaks["hbm_gbs"],
+                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json: bf16 burst, copy bandwidth)",
+                "frac_of_tensor_peak": round(achieved / peaks["bf16_tflops"], 4),
                 "kernel": "bi_gemm_kernel<bf16, out bf16, {}x{} tile on {} CTA(s), {} stages>".format(
                     g.config["block_m"], g.config["block_n"], g.config["ctas_per_tile"], g.config["stages"]),
-                "launch_timing": f"CUDA events around graphs of {REPS} launches per M, rotating cold copies "
+                "launch_timing": f"per M: CUDA events around graphs of {REPS} launches, rotating cold copies "
                                  "(us); the same with one copy, warm L2 where it fits (us_warm_l2)",
                 "hbm_regime_frac_M_le_64": min((r["frac"] for r in sweep if r["M"] <= 64), default=None),
                 "tensor_regime_frac_M_ge_2048": min((r["frac"] for r in sweep if r["M"] >= 2048), default=None)}
 
-    e2e = measure_e2e(g, W_np, X_np, args, dev, world) if not args.only_m else None
+    e2e = measure_e2e(g, W_np, X_np, args, dev, world)
     paths = measure_other_paths(dev, peaks) if not args.no_paths else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        fl, sec, desc = oracle_sample(args.cpu_budget)
-        cpu = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc}
+        cores = os.cpu_count() or 1
+        fl, sec, desc = oracle_sample(args.cpu_budget / 2, threads=cores)
+        fl1, sec1, desc1 = oracle_sample(args.cpu_budget / 2, threads=1)
+        cpu = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "single_thread": {"value": fl1 / sec1 / 1e12, "cores": 1, "sample": desc1}}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -388,7 +444,7 @@ def run_ours(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_obj(world), "roofline": roofline, "sweep": sweep, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clk, "gpu_launches": nM * args.steps, "peaks": peaks, "paths": paths,
-        "kernel_ms_per_step": round(kernel_ms_total, 4),
+        "kernel_ms_per_step": round(kernel_ms_total, 4), "static_w": STATIC_W,
         "timing": "timed region: K replays of the 19-launch sweep captured in CUDA graphs (one per rotation "
                   "offset); eager_ms_per_step: the same sweep through eager per-call launches",
         "eager_ms_per_step": round(eager_ms, 4),
@@ -396,6 +452,42 @@ def run_ours(args, rank, world, local):
     g.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def measure_cublas_context(Xs, Ws, g, stream, reps=30):
+    """Context only, not a target: torch.matmul (cuBLAS, batch-variant) on the same launches,
+    timed the same way (graphs of `reps` launches over the rotating cold copies), and per M the
+    byte differences between rows 0..M-1 computed alone and the same rows of the full 8192-row
+    product, for torch.matmul and for this library."""
+    import torch
+    X0, W0 = Xs[0], Ws[0]
+    full_cublas = torch.matmul(X0, W0)
+    full_ours = g(X0, W0)
+    out = {}
+    for M in M_SWEEP:
+        y = torch.empty((M, N_DIM), dtype=torch.bfloat16, device=X0.device)
+        gm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gm):
+            for j in range(reps):
+                torch.matmul(Xs[j % len(Xs)][:M], Ws[j % len(Ws)], out=y)
+        gm.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            gm.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) / reps)
+        del gm
+        alone_c = torch.matmul(X0[:M], W0)
+        alone_o = g(X0[:M], W0)
+        diff_c = int((alone_c.view(torch.int16) != full_cublas[:M].view(torch.int16)).sum().item()) * 2
+        diff_o = int((alone_o.view(torch.int16) != full_ours[:M].view(torch.int16)).sum().item()) * 2
+        out[M] = {"cublas_us": round(statistics.median(ts) * 1e3, 2),
+                  "cublas_byte_diff_vs_rows_of_M8192": diff_c, "ours_byte_diff_vs_rows_of_M8192": diff_o}
+    return out
 
 
 def measure_e2e(g, W_np, X_np, args, dev, world):
@@ -705,139 +797,6 @@ def measure_rmsnorm(dev, peaks, bf):
             "note": "graph-timed; rotating (x, y) sets > 2x L2 for every M; small M is launch-latency-bound"}
 
 
-def run_attention_only(args):
-    """Launch only the decode attention (the bench path's shape) for one batch x context, eagerly:
-    --warmup + --steps calls.  For profiling; prints the average call time as one JSON line."""
-    import torch
-    from invariant_bi_gemm_gb300 import BiAttention
-
-    dev = torch.device("cuda", 0)
-    B, L = (int(v) for v in args.attention_only.split(","))
-    a = ATTN
-    pages_per = (L + a["page_size"] - 1) // a["page_size"]
-    P = B * pages_per
-    g = torch.Generator(device=dev).manual_seed(1234)
-    shape = (P, a["page_size"], a["num_kv_heads"], a["head_dim"])
-    kc = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
-    vc = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
-    table = torch.randperm(P, generator=g, device=dev).to(torch.int32).view(B, pages_per).contiguous()
-    q = torch.randn((B, a["num_q_heads"], a["head_dim"]), generator=g, device=dev).to(torch.bfloat16)
-    q_seq = torch.arange(B, dtype=torch.int32, device=dev)
-    q_pos = torch.full((B,), L - 1, dtype=torch.int32, device=dev)
-    o = torch.empty_like(q)
-    attn = BiAttention(a["num_q_heads"], a["num_kv_heads"], a["head_dim"], a["page_size"], split_size=a["split_size"])
-    for _ in range(args.warmup):
-        attn(q, q_seq, q_pos, kc, vc, table, L - 1, o)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        attn(q, q_seq, q_pos, kc, vc, table, L - 1, o)
-    e1.record()
-    torch.cuda.synchronize()
-    t = e0.elapsed_time(e1) / 1e3 / max(1, args.steps)
-    err = attn.device_error()
-    print(json.dumps({"attention_only": [B, L], "us_per_call": round(t * 1e6, 2),
-                      "gbs": round(attention_bytes(B, L) / t / 1e9, 1), "device_error": err}))
-    attn.close()
-    if err != 0:
-        sys.exit(1)
-
-
-def run_prenorm_only(args):
-    """Launch only the mHC pre-norm projection (K = 16384, N = 24) at one M, eagerly: --warmup +
-    --steps calls.  For profiling; prints the average call time as one JSON line."""
-    import numpy as np
-    import torch
-
-    import inputgen as ig
-    from invariant_bi_gemm_gb300 import BiPreNorm
-
-    dev = torch.device("cuda", 0)
-    M, K, N = args.prenorm_only_m, 16384, 24
-    x = torch.from_numpy(ig.scaled_rows_bf16(ig.SEED_X, M, K).view(np.int16)).to(dev).view(torch.bfloat16)
-    w = torch.from_numpy(ig.normal_bf16(ig.SEED_W, K, N, std=0.02).view(np.int16)).to(dev).view(torch.bfloat16)
-    y = torch.empty((M, N), dtype=torch.float32, device=dev)
-    h = BiPreNorm(K, N, 1e-6)
-    for _ in range(args.warmup):
-        h(x, w, y)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        h(x, w, y)
-    e1.record()
-    torch.cuda.synchronize()
-    t = e0.elapsed_time(e1) / 1e3 / max(1, args.steps)
-    print(json.dumps({"prenorm_only_m": M, "us_per_call": round(t * 1e6, 2)}))
-    h.close()
-
-
-def run_rmsnorm_only(args):
-    """Launch only the RMSNorm (d = 4096) at one M, eagerly: --warmup + --steps launches.  For
-    profiling; prints the average launch time as one JSON line (not the benchmark line)."""
-    import numpy as np
-    import torch
-
-    import inputgen as ig
-    from invariant_bi_gemm_gb300 import BiRmsNorm
-
-    dev = torch.device("cuda", 0)
-    M = args.rmsnorm_only_m
-    x = torch.from_numpy(ig.scaled_rows_bf16(ig.SEED_X, M, RMS_D).view(np.int16)).to(dev).view(torch.bfloat16)
-    gw = torch.from_numpy(ig.rmsnorm_weight_bf16(ig.SEED_W, RMS_D).view(np.int16)).to(dev).view(torch.bfloat16)
-    y = torch.empty_like(x)
-    n = BiRmsNorm(RMS_D, RMS_EPS)
-    for _ in range(args.warmup):
-        n(x, gw, y)
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(args.steps):
-        n(x, gw, y)
-    b.record()
-    torch.cuda.synchronize()
-    t = a.elapsed_time(b) / 1e3 / max(1, args.steps)
-    print(json.dumps({"rmsnorm_only_m": M, "d": RMS_D, "us_per_launch": round(t * 1e6, 2),
-                      "gbs": round(rmsnorm_bytes(M) / t / 1e9, 1)}))
-    n.close()
-
-
-def run_mxfp8_only(args):
-    """Launch only the MXFP8 LLM-shape GEMM (E4M3 x[M,4096]·W[4096,14336], K-varying E8M0
-    scales, bf16 out) at one M, eagerly: --warmup + --steps launches.  For profiling; prints the
-    average launch time as one JSON line (not the benchmark line)."""
-    import torch
-
-    import inputgen as ig
-    from invariant_bi_gemm_gb300 import BiGemm
-
-    dev = torch.device("cuda", 0)
-    M = args.mxfp8_only_m
-    x8 = torch.from_numpy(ig.normal_e4m3(ig.SEED_X, M, K_DIM)).to(dev)
-    sx = torch.from_numpy(ig.e8m0_scales("VAR", ig.SEED_X, M, K_DIM // 32)).to(dev)
-    w8 = torch.from_numpy(ig.normal_e4m3(ig.SEED_W, K_DIM, N_DIM)).to(dev)
-    sw = torch.from_numpy(ig.e8m0_scales("VAR", ig.SEED_W, K_DIM // 32, N_DIM)).to(dev)
-    y = torch.empty((M, N_DIM), dtype=torch.bfloat16, device=dev)
-    g = BiGemm(K_DIM, N_DIM, "mxfp8")
-    for _ in range(args.warmup):
-        g(x8, w8, y, sx=sx, sw=sw)
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(args.steps):
-        g(x8, w8, y, sx=sx, sw=sw)
-    b.record()
-    torch.cuda.synchronize()
-    t = a.elapsed_time(b) / 1e3 / max(1, args.steps)
-    err = g.device_error()
-    print(json.dumps({"mxfp8_only_m": M, "us_per_launch": round(t * 1e6, 2),
-                      "tflops": round(flops(M) / t / 1e12, 1), "device_error": err}))
-    g.close()
-    if err != 0:
-        sys.exit(1)
-
-
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -847,33 +806,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-paths", action="store_true")
-    ap.add_argument("--only-m", type=int, default=0,
-                    help="time a single M of the sweep only (for profiling); skips e2e, paths, CPU")
-    ap.add_argument("--attention-only", default="",
-                    help="profiling aid: 'B,L' launches only the decode attention for batch B, context L, and exits")
-    ap.add_argument("--prenorm-only-m", type=int, default=0,
-                    help="profiling aid: launch only the mHC pre-norm projection at this M, eagerly, and exit")
-    ap.add_argument("--rmsnorm-only-m", type=int, default=0,
-                    help="profiling aid: launch only the RMSNorm (d = 4096) at this M, eagerly, and exit")
-    ap.add_argument("--mxfp8-only-m", type=int, default=0,
-                    help="launch only the MXFP8 LLM-shape GEMM at this M (for profiling)")
     args = ap.parse_args()
-    if args.mxfp8_only_m:
-        run_mxfp8_only(args)
-        return
-    if args.rmsnorm_only_m:
-        run_rmsnorm_only(args)
-        return
-    if args.attention_only:
-        run_attention_only(args)
-        return
-    if args.prenorm_only_m:
-        run_prenorm_only(args)
-        return
-    if args.only_m:
-        global M_SWEEP
-        M_SWEEP = [args.only_m]
-        args.no_cpu = args.no_paths = True
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_init()

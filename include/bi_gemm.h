@@ -92,7 +92,17 @@ typedef struct {
                              count (1 <= split_k <= ceil(K / BK)); still never M-dependent */
   int32_t max_ctas;       /* 0 = one CTA per SM; otherwise an upper bound on the grid     */
   uint64_t timeout_ns;    /* 0 = default (5 s); limit of every in-kernel wait             */
+  uint32_t flags;         /* OR of BI_GEMM_FLAG_* below; 0 = none                          */
+  uint32_t reserved;      /* must be 0                                                     */
 } bi_gemm_options;
+
+/* BI_GEMM_FLAG_STATIC_W: the caller guarantees that no kernel which may still be running when
+ * a run is queued writes that run's W (typical for inference weights).  Each run then starts
+ * loading its first W tiles while the previous kernel in the stream is still finishing, and
+ * only the x loads wait for that kernel (programmatic dependent launch); this hides part of
+ * the launch latency of back-to-back runs.  It changes no arithmetic and no result.  Without
+ * the flag every global load of a run waits for the previous kernel to complete. */
+#define BI_GEMM_FLAG_STATIC_W 1u
 
 /* bi_gemm_create with explicit options (NULL = defaults, same as bi_gemm_create). */
 int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtype, int scale_layout,
@@ -117,16 +127,20 @@ int bi_gemm_run(bi_gemm_t h, const void* x, int64_t M, const void* W,
  * difference is where a split count S > 1 keeps its scratch (one uint32 arrival counter per
  * output tile and tiles*S*128*BN fp32 partials): instead of the handle's workspace, grown with
  * cudaMallocAsync, it uses one fixed 8 MiB device array compiled into the library (4 KiB of
- * counters, so at most 1024 output tiles, then 8 MiB - 4 KiB of partials).  Every GPU on which
+ * counters, then 8 MiB - 4 KiB of partials).  Every GPU on which
  * the library's kernels are loaded holds that array until the process exits.  This call makes
  * no cudaMalloc, cudaMallocAsync or cudaFree and calls no allocating library routine.
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- *     with that device current) and remembers it; make that first call before any stream
- *     capture.  The handle's device must be current (else BI_GEMM_ERR_INVALID_ARG).
+ *   - The first call in each CUDA context looks up the array's device address there
+ *     (cudaGetSymbolAddress, with the handle's device current) and keeps it with the
+ *     context's unique id; later calls in that context reuse it, and a context created later
+ *     (for instance after cudaDeviceReset, which reloads the module) gets a fresh lookup.
+ *     Make that first call before any stream capture.  The handle's device must be current
+ *     (else BI_GEMM_ERR_INVALID_ARG).
  *   - A run whose scratch would not fit returns BI_GEMM_ERR_SCRATCH_LIMIT and queues nothing:
- *     the 128-row sub-tiles, tiles = ceil(M/block_m) * ctas_per_tile * ceil(N/BN), must be
- *     <= 1024 and tiles*S*128*BN*4 bytes must be <= 8 MiB - 4 KiB (bi_gemm_get_config gives
- *     block_m, ctas_per_tile, S and BN).  Handles with S == 1 use no scratch.
+ *     tiles*S*128*BN*4 bytes of partials must be <= 8 MiB - 4 KiB, where tiles, the 128-row
+ *     sub-tiles, is ceil(M/block_m) * ctas_per_tile * ceil(N/BN) (bi_gemm_get_config gives
+ *     block_m, ctas_per_tile, S and BN).  This is the bound that binds: it admits at most 127
+ *     sub-tiles, and the 4 KiB of counters hold 1024.  Handles with S == 1 use no scratch.
  *   - All calls in the process share the one array per device and it keeps the last call's
  *     contents; each call first clears, on `stream`, the counters it uses.  Calls whose work
  *     overlaps on the GPU (other streams, other threads, other handles) race on the array and

@@ -23,6 +23,7 @@ BI_BF16_OUT_F32 = 1
 BI_MXFP8E4M3_OUT_BF16 = 2
 BI_SCALES_NONE = 0
 BI_SCALES_E8M0_K32 = 1
+BI_GEMM_FLAG_STATIC_W = 1
 
 BI_GEMM_OK = 0
 BI_GEMM_ERR_INVALID_ARG = -1
@@ -59,7 +60,8 @@ class bi_gemm_scales(ctypes.Structure):
 
 
 class bi_gemm_options(ctypes.Structure):
-    _fields_ = [("split_k", ctypes.c_int32), ("max_ctas", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64)]
+    _fields_ = [("split_k", ctypes.c_int32), ("max_ctas", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
+                ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
 class bi_gemm_config(ctypes.Structure):
@@ -300,13 +302,14 @@ class BiGemm:
     """
 
     def __init__(self, K: int, N: int, kind: str = "bf16", split_k: int = 0, max_ctas: int = 0,
-                 timeout_ns: int = 0):
+                 timeout_ns: int = 0, static_w: bool = False):
         self.K, self.N, self.kind = int(K), int(N), kind
         self.dtype = _DTYPES[kind]
         layout = BI_SCALES_E8M0_K32 if kind == "mxfp8" else BI_SCALES_NONE
         opts = None
-        if split_k or max_ctas or timeout_ns:
-            opts = bi_gemm_options(int(split_k), int(max_ctas), int(timeout_ns))
+        flags = BI_GEMM_FLAG_STATIC_W if static_w else 0
+        if split_k or max_ctas or timeout_ns or flags:
+            opts = bi_gemm_options(int(split_k), int(max_ctas), int(timeout_ns), flags, 0)
         self.handle = bi_gemm_create(self.K, self.N, self.dtype, layout, opts)
 
     @property

@@ -150,6 +150,7 @@ struct bi_gemm {
   int device = 0, num_sms = 0, max_ctas = 0;
   int split = 1, kblocks = 0, n_tiles = 0;
   int max_groups = 0;      // CTA groups (single CTAs or pairs) resident at once
+  uint32_t flags = 0;      // BI_GEMM_FLAG_*
   uint64_t timeout_ns = kDefaultTimeoutNs;
   KernelInfo kern;
   uint32_t* d_status = nullptr;
@@ -297,6 +298,7 @@ int launch_core(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_ge
   p.a_box_rows = int32_t(a_box_rows);
   const int64_t x_bytes = M * h->K * (fp8 ? 1 : 2);
   p.group_n = int32_t(x_bytes <= kRasterXResidentBytes ? 1 : std::min<int64_t>(kRasterGroupN, h->n_tiles));
+  p.w_early = (h->flags & BI_GEMM_FLAG_STATIC_W) ? 1 : 0;
   p.timeout_ns = h->timeout_ns;
   p.test_flags = test_flags;
 
@@ -378,7 +380,8 @@ BI_GEMM_API int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtyp
   if (rc != BI_GEMM_OK) return rc;
   const int bk = dtype == BI_MXFP8E4M3_OUT_BF16 ? 128 : 64;
   const int64_t kblocks = (K + bk - 1) / bk;
-  if (opt && (opt->split_k < 0 || opt->split_k > kblocks || opt->max_ctas < 0))
+  if (opt && (opt->split_k < 0 || opt->split_k > kblocks || opt->max_ctas < 0 ||
+              (opt->flags & ~BI_GEMM_FLAG_STATIC_W) != 0u || opt->reserved != 0u))
     return BI_GEMM_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -413,6 +416,7 @@ BI_GEMM_API int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtyp
   h->n_tiles = int(n_tiles);
   h->split = (opt && opt->split_k > 0) ? opt->split_k : auto_split(n_tiles, kblocks, sms);
   h->timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+  h->flags = opt ? opt->flags : 0u;
   if (cudaFuncSetAttribute(h->kern.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->kern.smem) !=
           cudaSuccess ||
       cudaMalloc(&h->d_status, sizeof(uint32_t)) != cudaSuccess ||
@@ -553,32 +557,67 @@ BI_GEMM_API int bi_gemm_version(void) { return kVersion; }
 //
 // The array is kNoAllocScratchBytes per device; every GPU on which this library's kernels are
 // loaded holds it until the process exits.  Host code may not use the array's name as a device
-// address (it is a host-side stand-in); the device address is fetched once per device with
-// cudaGetSymbolAddress, with that device current, on the first bi_gemm_run_noalloc call there.
+// address (it is a host-side stand-in); the device address is fetched with cudaGetSymbolAddress,
+// with the device current, by the first bi_gemm_run_noalloc call in each CUDA context, and kept
+// with that context's unique id: a context created later (after cudaDeviceReset, say, where the
+// module is loaded again and the array may sit elsewhere) gets its own lookup.
 
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;     // 8 MiB per device
-constexpr size_t kNoAllocCounterBytes = 4096;                // arrival counters, <= 1024 tiles
+// Arrival counters first.  The partials bound is the one that binds: the smallest partial
+// block of a sub-tile (S = 2, BN = 64) is 64 KiB, so at most 127 sub-tiles fit beside the
+// counters, far fewer than the 1024 counters these 4 KiB hold.
+constexpr size_t kNoAllocCounterBytes = 4096;
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
 
+struct NoAllocSlot {
+  unsigned long long ctx_id = 0;   // id of the context the address belongs to
+  void* ptr = nullptr;
+};
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+NoAllocSlot g_noalloc[kNoAllocMaxDevices];
+
+// The current context's unique id (cuCtxGetId), or false when no context is current.
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext c = nullptr;
+  if (!get_cur || !get_id || get_cur(&c) != CUDA_SUCCESS || !c) return false;
+  return get_id(c, id) == CUDA_SUCCESS;
+}
 
 int noalloc_scratch_address(int dev, char** out) {
   if (dev < 0 || dev >= kNoAllocMaxDevices) return BI_GEMM_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  NoAllocSlot& slot = g_noalloc[dev];
+  unsigned long long id = 0;
+  const bool have_ctx = current_context_id(&id);
+  if (!have_ctx || !slot.ptr || slot.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
       return BI_GEMM_ERR_CUDA;
     }
-    g_noalloc_ptr[dev] = p;
+    // the lookup has made the device's context current if none was
+    if (!current_context_id(&id)) return BI_GEMM_ERR_CUDA;
+    slot.ptr = p;
+    slot.ctx_id = id;
   }
-  *out = static_cast<char*>(g_noalloc_ptr[dev]);
+  *out = static_cast<char*>(slot.ptr);
   return BI_GEMM_OK;
 }
 

@@ -71,6 +71,7 @@ struct KParams {
   int32_t coop_merge;       // S > 1, every unit has its own resident CTA group and the merge is
                             // large: the S split CTAs of a sub-tile share it (else the last to
                             // arrive merges alone)
+  int32_t w_early;          // W may be loaded before the previous kernel in the stream completes
   uint64_t timeout_ns;
   uint32_t test_flags;      // only read by the control build
 };
@@ -354,57 +355,85 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_par = 0;   // per stage: an issue is outstanding / its parity
-        bool ok = true, dep_done = false;
+        bool ok = true;
+        // Issue the loads of one k-block into stage `st`: with `w_part` the stage's byte count and
+        // the W tiles, with `x_part` the x tile.
+        auto issue = [&](int st, const UnitCoord& uc, int kb, bool w_part, bool x_part) {
+          const uint32_t fb = full_bar(st);
+          const uint32_t adst = sbase + C::OFF_A + st * C::A_BYTES;
+          const uint32_t bdst = sbase + C::OFF_B + st * C::B_BYTES;
+          const int row0 = uc.m_tile * C::TILE_M + int(rank) * kBM;
+          const int col0 = uc.n_tile * C::BN + int(rank) * C::BN_CTA;
+          // x rows at or past M are never stored, so they need not be loaded: a CTA whose 128
+          // rows all lie past M skips its x tile, and the x box is only as tall as M needs.
+          // The shared-memory rows left unwritten feed only those discarded output rows.
+          const uint32_t a_bytes = uint32_t(p.a_box_rows) * 128u;
+          const bool load_a = row0 < p.M;
+          if constexpr (kPair) {
+            const uint32_t lfb = ptx::mapa_shared(fb, 0);   // the leader's full barrier
+            if (w_part && rank == 0) {
+              const bool peer_a = row0 + kBM < p.M;
+              ptx::mbar_arrive_expect_tx(fb, (load_a ? a_bytes : 0u) + (peer_a ? a_bytes : 0u) +
+                                                 uint32_t(C::CTAS * C::B_BYTES));
+            }
+            if (x_part && load_a) ptx::tma_load_2d_pair(adst, &tmap_x, lfb, kb * C::BK, row0);
+            if (w_part) {
+  #pragma unroll
+              for (int a = 0; a < C::N_ATOMS; ++a)
+                ptx::tma_load_2d_pair(bdst + a * C::B_ATOM_BYTES, &tmap_w, lfb, col0 + a * C::ATOM_N,
+                                      kb * C::BK);
+            }
+          } else {
+            if (w_part) ptx::mbar_arrive_expect_tx(fb, a_bytes + uint32_t(C::B_BYTES));
+            if (x_part) ptx::tma_load_2d(adst, &tmap_x, fb, kb * C::BK, row0);
+            if (w_part) {
+  #pragma unroll
+              for (int a = 0; a < C::N_ATOMS; ++a)
+                ptx::tma_load_2d(bdst + a * C::B_ATOM_BYTES, &tmap_w, fb, col0 + a * C::ATOM_N, kb * C::BK);
+            }
+          }
+          issued_mask |= 1u << st;
+          issued_par = (issued_par & ~(1u << st)) | (phase << st);
+        };
+        // W is only read.  When the caller has declared that no kernel which may still be running
+        // writes it (p.w_early), the W tiles of this CTA's first STAGES k-blocks are issued before
+        // the wait for the previous kernel in the stream; only x (which may be that kernel's
+        // output) and every later load wait for it.  The stages are fresh, so no empty-barrier
+        // wait is needed for them.
+        int pre = 0;
+        bool early = p.w_early != 0;
+  #ifdef BI_GEMM_CONTROLS
+        early = early && !(p.test_flags & 1u);
+  #endif
+        if (early) {
+          for (int u = group; u < units && pre < C::STAGES; u += ngroups) {
+            const UnitCoord uc = unit_coord(u, p);
+            for (int kb = uc.kb_begin; kb < uc.kb_end && pre < C::STAGES; ++kb, ++pre)
+              issue(pre, uc, kb, true, false);
+          }
+  #ifdef BI_GEMM_TRIGGER_EARLY
+          ptx::launch_dependents();
+  #endif
+        }
+        ptx::grid_dependency_wait();
+        int item = 0;
         for (int u = group; u < units && ok; u += ngroups) {
           const UnitCoord uc = unit_coord(u, p);
-          for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
-            if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
-              ok = false;
-              break;
-            }
-            if (!dep_done) {
-              ptx::grid_dependency_wait();
-              dep_done = true;
-            }
-            bool skip = false;
-  #ifdef BI_GEMM_CONTROLS
-            // control build only: withhold one stage so that the consumer's bounded wait expires
-            skip = (p.test_flags & 1u) && u == group && kb == uc.kb_begin;
-  #endif
-            if (!skip) {
-              const uint32_t fb = full_bar(stage);
-              const uint32_t adst = sbase + C::OFF_A + stage * C::A_BYTES;
-              const uint32_t bdst = sbase + C::OFF_B + stage * C::B_BYTES;
-              const int row0 = uc.m_tile * C::TILE_M + int(rank) * kBM;
-              const int col0 = uc.n_tile * C::BN + int(rank) * C::BN_CTA;
-              // x rows at or past M are never stored, so they need not be loaded: a CTA whose 128
-              // rows all lie past M skips its x tile, and the x box is only as tall as M needs.
-              // The shared-memory rows left unwritten feed only those discarded output rows.
-              const uint32_t a_bytes = uint32_t(p.a_box_rows) * 128u;
-              const bool load_a = row0 < p.M;
-              if constexpr (kPair) {
-                const uint32_t lfb = ptx::mapa_shared(fb, 0);   // the leader's full barrier
-                if (rank == 0) {
-                  const bool peer_a = row0 + kBM < p.M;
-                  ptx::mbar_arrive_expect_tx(fb, (load_a ? a_bytes : 0u) + (peer_a ? a_bytes : 0u) +
-                                                     uint32_t(C::CTAS * C::B_BYTES));
-                }
-                if (load_a) ptx::tma_load_2d_pair(adst, &tmap_x, lfb, kb * C::BK, row0);
-  #pragma unroll
-                for (int a = 0; a < C::N_ATOMS; ++a)
-                  ptx::tma_load_2d_pair(bdst + a * C::B_ATOM_BYTES, &tmap_w, lfb, col0 + a * C::ATOM_N,
-                                        kb * C::BK);
-              } else {
-                ptx::mbar_arrive_expect_tx(fb, a_bytes + uint32_t(C::B_BYTES));
-                ptx::tma_load_2d(adst, &tmap_x, fb, kb * C::BK, row0);
-  #pragma unroll
-                for (int a = 0; a < C::N_ATOMS; ++a)
-                  ptx::tma_load_2d(bdst + a * C::B_ATOM_BYTES, &tmap_w, fb, col0 + a * C::ATOM_N, kb * C::BK);
+          for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb, ++item) {
+            if (item < pre) {
+              issue(stage, uc, kb, false, true);          // its W is already on the way
+            } else {
+              if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
+                ok = false;
+                break;
               }
-              issued_mask |= 1u << stage;
-              issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+              bool skip = false;
+  #ifdef BI_GEMM_CONTROLS
+              // control build only: withhold one stage so that the consumer's bounded wait expires
+              skip = (p.test_flags & 1u) && u == group && kb == uc.kb_begin;
+  #endif
+              if (!skip) issue(stage, uc, kb, true, true);
             }
-
             if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;

@@ -225,7 +225,8 @@ def _structs(header):
 def test_binding_structs_match_the_headers(header, name, cls):
     """The ctypes structures of the binding list the header's fields in the header's order with
     the header's widths, so a field added on one side only is caught without a GPU."""
-    width = {"int32_t": ctypes.c_int32, "uint64_t": ctypes.c_uint64, "int64_t": ctypes.c_int64}
+    width = {"int32_t": ctypes.c_int32, "uint32_t": ctypes.c_uint32, "uint64_t": ctypes.c_uint64,
+             "int64_t": ctypes.c_int64}
     fields = _structs(header)[name]
     py = getattr(bg, cls)._fields_
     assert [n for _, n in fields] == [n for n, _ in py]
