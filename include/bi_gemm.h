@@ -118,6 +118,29 @@ int bi_gemm_create_ex(bi_gemm_t* out, int64_t K, int64_t N, int dtype, int scale
 int bi_gemm_run(bi_gemm_t h, const void* x, int64_t M, const void* W,
                 const bi_gemm_scales* scales, void* y, void* stream);
 
+/* One row block of a gathered run: x [rows, K] (device pointer, 16-byte aligned, rows contiguous)
+ * and, for MXFP8, its scales sx [rows, K/32] (device pointer, 4-byte aligned; NULL for bf16). */
+typedef struct {
+  const void* x;
+  const uint8_t* sx;
+  int64_t rows;
+} bi_gemm_block;
+
+/* Gather + GEMM: the all-gather matmul of the batch-invariance test issue ("Background": each
+ * rank's row block of x is gathered, then multiplied by the shared W, and the defect was one
+ * kernel for the local rows and another for the gathered ones).  The nblocks blocks, in order
+ * (say rank 0's, rank 1's, ...; all in this GPU's memory: in a multi-rank run the caller's
+ * collective has delivered them), are copied into x_out [M, K], M = the sum of their rows (and,
+ * for MXFP8, their scales into sx_out [M, K/32]); then y [M, N] = x_out · W runs on the handle
+ * exactly as bi_gemm_run, with its one kernel configuration for every row.  So a row's output bits
+ * do not depend on which block it came from or on the other blocks, and equal those of
+ * bi_gemm_run on its block alone.  sw: W's scales [K/32, N] for MXFP8 (16-byte aligned), NULL for
+ * bf16.  1 <= nblocks <= 256; a block may have 0 rows.  x_out (16-byte aligned) and sx_out
+ * (4-byte aligned) are caller-owned and must not overlap the blocks.  Asynchronous on `stream`;
+ * errors as bi_gemm_run, and BI_GEMM_ERR_INVALID_ARG for a bad block table. */
+int bi_gemm_run_gathered(bi_gemm_t h, const bi_gemm_block* blocks, int32_t nblocks, void* x_out,
+                         uint8_t* sx_out, const void* W, const uint8_t* sw, void* y, void* stream);
+
 /* Allocation-free variant of bi_gemm_run (the papers have no counterpart; this is a service
  * of this library).  It is for callers that may not allocate device memory when they run a
  * GEMM: code whose device memory is wholly owned and budgeted by another framework's pool,

@@ -38,7 +38,7 @@ BI_GEMM_ERR_SCRATCH_LIMIT = -7
 EXPORTED_SYMBOLS = (
     "bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_get_device_error",
     "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_strerror",
-    "bi_gemm_version", "bi_gemm_run_noalloc",
+    "bi_gemm_version", "bi_gemm_run_noalloc", "bi_gemm_run_gathered",
 )
 # every symbol include/bi_rmsnorm.h declares
 RMSNORM_EXPORTED_SYMBOLS = ("bi_rmsnorm_create", "bi_rmsnorm_run", "bi_rmsnorm_get_config", "bi_rmsnorm_destroy")
@@ -57,6 +57,10 @@ class BiGemmError(RuntimeError):
 
 class bi_gemm_scales(ctypes.Structure):
     _fields_ = [("sx", ctypes.c_void_p), ("sw", ctypes.c_void_p)]
+
+
+class bi_gemm_block(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("sx", ctypes.c_void_p), ("rows", ctypes.c_int64)]
 
 
 class bi_gemm_options(ctypes.Structure):
@@ -96,6 +100,7 @@ def _load() -> ctypes.CDLL:
     L.bi_gemm_create_ex.argtypes = [ctypes.POINTER(P), I64, I64, I32, I32, ctypes.POINTER(bi_gemm_options)]
     L.bi_gemm_run.argtypes = [P, P, I64, P, ctypes.POINTER(bi_gemm_scales), P, P]
     L.bi_gemm_run_noalloc.argtypes = [P, P, I64, P, ctypes.POINTER(bi_gemm_scales), P, P]
+    L.bi_gemm_run_gathered.argtypes = [P, ctypes.POINTER(bi_gemm_block), ctypes.c_int32, P, P, P, P, P, P]
     L.bi_gemm_get_device_error.argtypes = [P, P]
     L.bi_gemm_destroy.argtypes = [P]
     L.bi_gemm_get_config.argtypes = [P, ctypes.POINTER(bi_gemm_config)]
@@ -117,7 +122,8 @@ def _load() -> ctypes.CDLL:
     L.bi_prenorm_run.argtypes = [P, P, I64, P, P, P]
     L.bi_prenorm_get_config.argtypes = [P, ctypes.POINTER(bi_prenorm_config)]
     L.bi_prenorm_destroy.argtypes = [P]
-    for n in ("bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_run_noalloc", "bi_gemm_get_device_error",
+    for n in ("bi_gemm_create", "bi_gemm_create_ex", "bi_gemm_run", "bi_gemm_run_noalloc", "bi_gemm_run_gathered",
+              "bi_gemm_get_device_error",
               "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_version") + \
             RMSNORM_EXPORTED_SYMBOLS + ATTENTION_EXPORTED_SYMBOLS + PRENORM_EXPORTED_SYMBOLS:
         getattr(L, n).restype = I32
@@ -353,6 +359,48 @@ class BiGemm:
 
     __call__ = run
 
+    def run_gathered(self, blocks, W, x_out=None, y=None, sx_blocks=None, sx_out=None, sw=None, stream=None):
+        """y = concat(blocks) · W through bi_gemm_run_gathered: the row blocks (contiguous [rows, K]
+        CUDA tensors, in order; for MXFP8 with their scales sx_blocks) are gathered into x_out
+        (and sx_out), then multiplied with the same kernel configuration as every other row.
+        Returns (y, x_out, sx_out)."""
+        import torch
+        nb = len(blocks)
+        if nb < 1 or (sx_blocks is not None and len(sx_blocks) != nb):
+            raise ValueError("one or more blocks (and one scale block per block for MXFP8)")
+        fp8 = self.kind == "mxfp8"
+        for b in blocks:
+            if b.dim() != 2 or b.shape[1] != self.K or not (b.is_cuda and b.is_contiguous()):
+                raise ValueError("blocks must be contiguous [rows, K] CUDA tensors")
+        M = sum(int(b.shape[0]) for b in blocks)
+        dev = blocks[0].device
+        if x_out is None:
+            x_out = torch.empty((M, self.K), dtype=blocks[0].dtype, device=dev)
+        if fp8:
+            if sx_blocks is None or sw is None:
+                raise ValueError("MXFP8 needs sx_blocks and sw")
+            if sx_out is None:
+                sx_out = torch.empty((M, self.K // 32), dtype=torch.uint8, device=dev)
+        if y is None:
+            y = torch.empty((M, self.N), dtype=self.out_dtype(), device=dev)
+        if tuple(x_out.shape) != (M, self.K) or tuple(y.shape) != (M, self.N):
+            raise ValueError("x_out [M, K] and y [M, N] expected")
+        arr = (bi_gemm_block * nb)()
+        for i, b in enumerate(blocks):
+            arr[i].x = b.data_ptr()
+            arr[i].sx = sx_blocks[i].data_ptr() if fp8 else None
+            arr[i].rows = int(b.shape[0])
+        if stream is None:
+            stream = torch.cuda.current_stream(dev)
+        s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        rc = library().bi_gemm_run_gathered(ctypes.c_void_p(self.handle), arr, nb, ctypes.c_void_p(x_out.data_ptr()),
+                                            ctypes.c_void_p(sx_out.data_ptr() if fp8 else None),
+                                            ctypes.c_void_p(W.data_ptr()),
+                                            ctypes.c_void_p(sw.data_ptr() if fp8 else None),
+                                            ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(s))
+        _check(rc, "bi_gemm_run_gathered")
+        return y, x_out, sx_out
+
     def device_error(self, stream=None) -> int:
         s = 0
         if stream is not None:
@@ -540,5 +588,5 @@ __all__ = [
     "bi_rmsnorm_config", "RMSNORM_EXPORTED_SYMBOLS",
     "BiGemm", "BiGemmError", "bi_gemm_create", "bi_gemm_run", "bi_gemm_run_noalloc", "bi_gemm_get_device_error",
     "bi_gemm_destroy", "bi_gemm_get_config", "bi_gemm_workspace_size", "bi_gemm_strerror",
-    "bi_gemm_version", "bi_gemm_scales", "bi_gemm_options", "EXPORTED_SYMBOLS", "LIB_PATH", "library",
+    "bi_gemm_version", "bi_gemm_scales", "bi_gemm_options", "bi_gemm_block", "EXPORTED_SYMBOLS", "LIB_PATH", "library",
 ]

@@ -33,7 +33,8 @@ def nvcc() -> str:
 
 
 def _sources():
-    return glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
+    return (glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(ROOT, "include", "*.h")) +
+            glob.glob(os.path.join(ROOT, "tests", "include", "*.h")))
 
 
 def _stale(lib: str) -> bool:

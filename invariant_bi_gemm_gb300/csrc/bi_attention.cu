@@ -84,7 +84,7 @@ __device__ __forceinline__ bool named_bar_or1(bool pred) {
 
 constexpr int kThreads = 128;        // threads per block (four warps)
 constexpr int kStagePos = 64;        // positions per staged key / value tile
-constexpr int kMergeThreads = 1024;  // merge block: four threads per output pair
+constexpr int kMergeThreads = 256;   // merge block: four lanes per output pair, 64 pairs
 constexpr int kStages = 2;           // staging ring depth (more blocks per SM beat a deeper ring)
 constexpr int kDefaultSplit = 512;
 constexpr uint32_t kErrInput = 1u;   // bad q_seq / q_pos / page-table extent
@@ -110,6 +110,7 @@ struct Params {
   int32_t nstage;    // ring depth of the TMA variant
   int32_t stall_block;   // failure injection (test controls only): this block never issues its
                          // first load; -1 in the product
+  int32_t inline_plan;   // T <= kInlinePlanMaxT: the attention kernel derives unit records itself
   uint64_t timeout_ns;   // limit of its bounded waits
   float c;           // scale * log2(e)
 };
@@ -253,7 +254,69 @@ __device__ __forceinline__ Unit unit_from(const Params& p, const int4 rec) {
   return w;
 }
 
-template <int D, int G>
+// Small batches (T <= kInlinePlanMaxT tokens) skip the plan kernel: a warp derives a unit's
+// record from q_seq / q_pos itself, with the plan's numbering (tokens in order, a token's units
+// numbered split * Hkv + KV head, no units for a token the kernel cannot serve).  The tokens are
+// loaded first (plan_load) and scanned later (plan_find), so that the load latency
+// can overlap other work.
+constexpr int kInlinePlanMaxT = 32;
+
+struct PlanRegs {
+  int32_t b[kInlinePlanMaxT / 32 + 1], pos[kInlinePlanMaxT / 32 + 1];
+};
+
+__device__ __forceinline__ void plan_load(const Params& p, PlanRegs& r) {
+  const int lane = int(threadIdx.x) & 31;
+#pragma unroll
+  for (int k = 0; k < kInlinePlanMaxT / 32 + 1; ++k) {
+    const int64_t t = int64_t(k * 32 + lane);
+    r.b[k] = t < p.T ? p.q_seq[t] : -1;
+    r.pos[k] = t < p.T ? p.q_pos[t] : -1;
+  }
+}
+
+// Warp-collective (all 32 lanes): the record of unit u (x = -1 when u is past the last unit) and
+// the total number of units.  With `report`, tokens the kernel cannot serve set the status word.
+__device__ __forceinline__ int4 plan_find(const Params& p, const PlanRegs& r, int64_t u, int32_t* total,
+                                          bool report) {
+  const int lane = int(threadIdx.x) & 31;
+  int32_t carry = 0;
+  int4 rec = make_int4(-1, 0, 0, 0);
+#pragma unroll
+  for (int k = 0; k < kInlinePlanMaxT / 32 + 1; ++k) {
+    const int64_t t = int64_t(k * 32 + lane);
+    const int32_t b = r.b[k], pos = r.pos[k];
+    int32_t n = 0;
+    if (t < p.T) {
+      if (b < 0 || b >= p.B || pos < 0 || int64_t(pos / p.page_size) >= p.max_pages) {
+        if (report) atomicOr(p.status, kErrInput);
+      } else if (pos > p.max_pos) {
+        if (report) atomicOr(p.status, kErrBound);
+      } else {
+        n = splits_of(pos, p.split) * p.Hkv;
+      }
+    }
+    int32_t x = n;   // inclusive scan over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    const int32_t ex = carry + x - n;
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, n > 0 && u >= ex && u < int64_t(ex) + n);
+    if (hit) {
+      const int src = __ffs(int(hit)) - 1;
+      const int32_t e = __shfl_sync(0xFFFFFFFFu, ex, src);
+      rec = make_int4(k * 32 + src, __shfl_sync(0xFFFFFFFFu, b, src), __shfl_sync(0xFFFFFFFFu, pos, src),
+                      int32_t(u - e));
+    }
+    carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+  }
+  *total = carry;
+  return rec;
+}
+
+template <int D, int G, bool kInline>
 __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
   using C = Cfg<D, G>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -271,11 +334,31 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
   const bool row_ok = gq < G;
   const int dbase = warp * C::DW;               // this warp's output dimensions
 
-  ptx::grid_dependency_wait();   // the plan is complete and visible
+  ptx::grid_dependency_wait();   // the plan (or the previous kernel) is complete and visible
   ptx::launch_dependents();
-  const int32_t total = p.cum[p.T];
   int64_t u = blockIdx.x;
+  int32_t total = 0;
+  int4 rec0 = make_int4(0, 0, 0, 0);
+  if constexpr (kInline) {
+    PlanRegs pr;
+    plan_load(p, pr);
+    rec0 = plan_find(p, pr, u, &total, blockIdx.x == 0 && tid < 32);
+  } else {
+    total = p.cum[p.T];
+    if (u < total) rec0 = p.urec[u];
+  }
   if (u >= total) return;
+  // record of a later unit of this block
+  auto record = [&](int64_t w) {
+    if constexpr (!kInline) {
+      return p.urec[w];
+    } else {
+      PlanRegs pr;
+      int32_t tot;
+      plan_load(p, pr);
+      return plan_find(p, pr, w, &tot, false);
+    }
+  };
 
   // Element offset of each key / value row of a unit's split in the caches (without the KV head),
   // or -1 for a row whose page index is outside [0, num_pages).
@@ -329,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
     return stage + r * C::ROW_BYTES + ((c ^ (r & (C::CHUNKS - 1))) << 4);
   };
 
-  Unit cur = unit_from(p, p.urec[u]);
+  Unit cur = unit_from(p, rec0);
   int half = 0;
   load_q(cur, half);
   fill_rows(cur, half);
@@ -352,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
     Unit nxt;
     auto fetch_next = [&]() {
       if (has_next) {
-        nxt = unit_from(p, p.urec[un]);
+        nxt = unit_from(p, record(un));
         fill_rows(nxt, half ^ 1);
         load_q(nxt, half ^ 1);
       }
@@ -567,7 +650,7 @@ __device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, const P
   return true;
 }
 
-template <int D, int G>
+template <int D, int G, bool kInline>
 __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PER_SM)
     attn_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Params p) {
   using C = Cfg<D, G>;
@@ -600,10 +683,22 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
     ptx::prefetch_tensormap(&tmv);
   }
   __syncthreads();
-  ptx::grid_dependency_wait();   // the plan is complete and visible
+  ptx::grid_dependency_wait();   // the plan (or the previous kernel) is complete and visible
   ptx::launch_dependents();
-  const int32_t total = p.cum[p.T];
+  int32_t total = 0;
+  int4 rec0 = make_int4(0, 0, 0, 0);
+  if constexpr (kInline) {
+    PlanRegs pr;
+    plan_load(p, pr);
+    rec0 = plan_find(p, pr, int64_t(blockIdx.x), &total, blockIdx.x == 0 && warp == 0);
+  } else {
+    total = p.cum[p.T];
+    if (int64_t(blockIdx.x) < total) rec0 = p.urec[blockIdx.x];
+  }
   if (int64_t(blockIdx.x) >= total) return;
+  // The next unit's record is fetched in two steps a stage apart: the plan's table entry, or
+  // with the inline plan the tokens' positions (first step) and the warp's scan (second step).
+  PlanRegs npr;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -621,7 +716,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
     bool bad_page = false, stop = false;
     uint32_t seq = 0;   // loads issued
     int64_t u = blockIdx.x;
-    Unit cur = unit_from(p, p.urec[u]);
+    Unit cur = unit_from(p, rec0);
     int32_t pg[4];
     load_pages(cur, pg);
     while (!stop) {
@@ -633,8 +728,15 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
       const int nload = 2 * cur.nsub;
       const int npu = (cur.valid + ps - 1) / ps;
       for (int i = 0; i < nload; ++i, ++seq) {
-        if (i == 0 && has_next) nrec = p.urec[un];
+        if (i == 0 && has_next) {
+          if constexpr (kInline) plan_load(p, npr);
+          else nrec = p.urec[un];
+        }
         if (i == 1 && has_next) {
+          if constexpr (kInline) {
+            int32_t tot;
+            nrec = plan_find(p, npr, un, &tot, false);
+          }
           nxt = unit_from(p, nrec);
           load_pages(nxt, npg);
         }
@@ -709,7 +811,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
     }
   };
   int64_t u = blockIdx.x;
-  Unit cur = unit_from(p, p.urec[u]);
+  Unit cur = unit_from(p, rec0);
   uint32_t qr[TC::QW];
   load_q(cur, qr);
   uint32_t seq = 0;
@@ -744,8 +846,15 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
 #pragma unroll
     for (int n = 0; n < TC::NT2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
     for (int i = 0; i < nload; ++i, ++seq) {
-      if (i == 0 && has_next) nrec = p.urec[un];
+      if (i == 0 && has_next) {
+        if constexpr (kInline) plan_load(p, npr);
+        else nrec = p.urec[un];
+      }
       if (i == 1 && has_next) {
+        if constexpr (kInline) {
+          int32_t tot;
+          nrec = plan_find(p, npr, un, &tot, false);
+        }
         nxt = unit_from(p, nrec);
         load_q(nxt, qr);
       }
@@ -896,18 +1005,24 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PE
 
 // Merge of the splits of every (token, KV head) with more than one split, after all units.  The
 // n splits are cut into four consecutive groups of c = ceil(n / 4); every output pair of every
-// head is handled by four threads, one per group, so that the partial loads of a long split list
-// are spread over four times the threads.  Per output, with M = max_s m_s (exact):
+// head is handled by four consecutive lanes, one per group.  Per output, with M = max_s m_s (exact):
 //   L_q = sum_{s in group q, ascending} l_s 2^(m_s - M),  A_q = sum_{s in group q} acc_s 2^(m_s - M),
 //   L = ((L_0 + L_1) + L_2) + L_3,  A likewise,  o = A / L.
 // n depends only on the token's position, so the order is fixed for the token whatever the batch.
-template <int D, int G>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
+// A block covers kMergePairs output pairs of one (token, KV head); a lane loads the (m, l) pairs
+// and partial sums of up to kMergeBatch splits of its group in one batch before it uses them, so
+// that a context of up to 4 * kMergeBatch splits costs one round of loads.  Two instantiations
+// differ only in that batch (and so in registers and blocks per SM): 4 for short split lists,
+// where many resident blocks matter, 16 for long ones.  The arithmetic is the same.
+constexpr int kMergePairs = kMergeThreads / 4;
+
+template <int D, int G, int kMergeBatch>
+__global__ void __launch_bounds__(kMergeThreads, kMergeBatch <= 4 ? 4 : 2) merge_kernel(const Params p) {
   constexpr int kPairs = G * D / 2;
-  __shared__ float sm[kPairs][4];       // group maxima, then group sums of weights
-  __shared__ float2 sa[kPairs][4];      // group weighted sums
+  constexpr int kSlices = (kPairs + kMergePairs - 1) / kMergePairs;
   ptx::grid_dependency_wait();   // every unit's partial results are complete and visible
-  const int64_t job = blockIdx.x;                       // token * Hkv + KV head
+  const int64_t job = blockIdx.x / kSlices;             // token * Hkv + KV head
+  const int slice = int(blockIdx.x - job * kSlices);
   const int64_t t = job / p.Hkv;
   const int32_t kh = int32_t(job - t * p.Hkv);
   if (t >= p.T) return;
@@ -917,71 +1032,118 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
   if (n == 1 || pos > p.max_pos) return;    // written directly / refused by the plan
   const int64_t slot0 = job * int64_t(p.max_splits);
   const int32_t c = (n + 3) / 4;
-  for (int it = int(threadIdx.x); it < 4 * kPairs; it += kMergeThreads) {
-    const int pr = it >> 2, q = it & 3, g = pr / (D / 2);
-    const int32_t s0 = q * c, s1 = min(n, s0 + c);
-    float m = -INFINITY;
-#pragma unroll 8
-    for (int32_t ss = s0; ss < s1; ++ss) m = fmaxf(m, p.ml[((slot0 + ss) * G + g) * 2]);
-    sm[pr][q] = m;
-  }
-  __syncthreads();
-  float2 part[kPairs * 4 / kMergeThreads + 1];
-  float lpart[kPairs * 4 / kMergeThreads + 1];
-  int k = 0;
-  for (int it = int(threadIdx.x); it < 4 * kPairs; it += kMergeThreads, ++k) {
-    const int pr = it >> 2, q = it & 3, g = pr / (D / 2), d = (pr % (D / 2)) * 2;
-    const float M = fmaxf(fmaxf(sm[pr][0], sm[pr][1]), fmaxf(sm[pr][2], sm[pr][3]));
-    const int32_t s0 = q * c, s1 = min(n, s0 + c);
-    float L = 0.0f, A0 = 0.0f, A1 = 0.0f;
-#pragma unroll 8
-    for (int32_t ss = s0; ss < s1; ++ss) {
-      const float2 ml = *reinterpret_cast<const float2*>(p.ml + ((slot0 + ss) * G + g) * 2);
-      const float f = exp2f(__fsub_rn(ml.x, M));
-      L = __fadd_rn(L, __fmul_rn(ml.y, f));
-      const float2 v = *reinterpret_cast<const float2*>(p.part + ((slot0 + ss) * G + g) * D + d);
-      A0 = __fadd_rn(A0, __fmul_rn(v.x, f));
-      A1 = __fadd_rn(A1, __fmul_rn(v.y, f));
+  const int pr = slice * kMergePairs + int(threadIdx.x >> 2), q = int(threadIdx.x & 3);
+  const bool valid = pr < kPairs;                       // uniform over the four lanes of a pair
+  const int g = valid ? pr / (D / 2) : 0, d = valid ? (pr % (D / 2)) * 2 : 0;
+  const int32_t s0 = min(n, q * c), s1 = valid ? min(n, s0 + c) : s0;
+  const float* mlp = p.ml + (slot0 * G + g) * 2;        // split ss: mlp[ss * G * 2]
+  const float* pp = p.part + (slot0 * G + g) * D + d;   // split ss: pp[ss * G * D]
+  float L = 0.0f, A0 = 0.0f, A1 = 0.0f;
+  if (c <= kMergeBatch) {
+    float2 ml[kMergeBatch], v[kMergeBatch];
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i) {
+      if (s0 + i < s1) {
+        ml[i] = *reinterpret_cast<const float2*>(mlp + int64_t(s0 + i) * G * 2);
+        v[i] = *reinterpret_cast<const float2*>(pp + int64_t(s0 + i) * G * D);
+      }
     }
-    part[k] = make_float2(A0, A1);
-    lpart[k] = L;
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i)
+      if (s0 + i < s1) m = fmaxf(m, ml[i].x);
+    const float m1 = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));   // the pair's four lanes
+    const float M = fmaxf(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, 2));
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i) {
+      if (s0 + i < s1) {
+        const float f = exp2f(__fsub_rn(ml[i].x, M));
+        L = __fadd_rn(L, __fmul_rn(ml[i].y, f));
+        A0 = __fadd_rn(A0, __fmul_rn(v[i].x, f));
+        A1 = __fadd_rn(A1, __fmul_rn(v[i].y, f));
+      }
+    }
+  } else {
+    // longer contexts: the group maximum over batches of loads, then the sums batch by batch
+    float m = -INFINITY;
+    for (int32_t b0 = s0; b0 < s1; b0 += kMergeBatch) {
+      float mv[kMergeBatch];
+#pragma unroll
+      for (int i = 0; i < kMergeBatch; ++i)
+        mv[i] = b0 + i < s1 ? mlp[int64_t(b0 + i) * G * 2] : -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kMergeBatch; ++i) m = fmaxf(m, mv[i]);
+    }
+    const float m1 = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));   // the pair's four lanes
+    const float M = fmaxf(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, 2));
+    for (int32_t b0 = s0; b0 < s1; b0 += kMergeBatch) {
+      float2 ml[kMergeBatch], v[kMergeBatch];
+#pragma unroll
+      for (int i = 0; i < kMergeBatch; ++i) {
+        if (b0 + i < s1) {
+          ml[i] = *reinterpret_cast<const float2*>(mlp + int64_t(b0 + i) * G * 2);
+          v[i] = *reinterpret_cast<const float2*>(pp + int64_t(b0 + i) * G * D);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kMergeBatch; ++i) {
+        if (b0 + i < s1) {
+          const float f = exp2f(__fsub_rn(ml[i].x, M));
+          L = __fadd_rn(L, __fmul_rn(ml[i].y, f));
+          A0 = __fadd_rn(A0, __fmul_rn(v[i].x, f));
+          A1 = __fadd_rn(A1, __fmul_rn(v[i].y, f));
+        }
+      }
+    }
   }
-  __syncthreads();   // every group maximum has been read
-  k = 0;
-  for (int it = int(threadIdx.x); it < 4 * kPairs; it += kMergeThreads, ++k) {
-    sm[it >> 2][it & 3] = lpart[k];
-    sa[it >> 2][it & 3] = part[k];
+  // the four group sums of the pair, added in group order by the pair's first lane
+  const int base = int(threadIdx.x & 31) & ~3;
+  float Lq[4], A0q[4], A1q[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    Lq[k] = __shfl_sync(0xFFFFFFFFu, L, base + k);
+    A0q[k] = __shfl_sync(0xFFFFFFFFu, A0, base + k);
+    A1q[k] = __shfl_sync(0xFFFFFFFFu, A1, base + k);
   }
-  __syncthreads();
-  for (int pr = int(threadIdx.x); pr < kPairs; pr += kMergeThreads) {
-    const int g = pr / (D / 2), d = (pr % (D / 2)) * 2;
-    const float L = __fadd_rn(__fadd_rn(__fadd_rn(sm[pr][0], sm[pr][1]), sm[pr][2]), sm[pr][3]);
-    const float A0 = __fadd_rn(__fadd_rn(__fadd_rn(sa[pr][0].x, sa[pr][1].x), sa[pr][2].x), sa[pr][3].x);
-    const float A1 = __fadd_rn(__fadd_rn(__fadd_rn(sa[pr][0].y, sa[pr][1].y), sa[pr][2].y), sa[pr][3].y);
+  if (valid && q == 0) {
+    const float Ls = __fadd_rn(__fadd_rn(__fadd_rn(Lq[0], Lq[1]), Lq[2]), Lq[3]);
+    const float As0 = __fadd_rn(__fadd_rn(__fadd_rn(A0q[0], A0q[1]), A0q[2]), A0q[3]);
+    const float As1 = __fadd_rn(__fadd_rn(__fadd_rn(A1q[0], A1q[1]), A1q[2]), A1q[3]);
     *reinterpret_cast<uint32_t*>(p.o + (t * p.Hq + int64_t(kh) * G + g) * D + d) =
-        pack_bf16x2(__fdiv_rn(A0, L), __fdiv_rn(A1, L));
+        pack_bf16x2(__fdiv_rn(As0, Ls), __fdiv_rn(As1, Ls));
   }
 }
+
+template <int D, int G>
+constexpr int merge_slices_of() { return (G * D / 2 + kMergePairs - 1) / kMergePairs; }
 
 struct KernelInfo {
   const void* fn = nullptr;
   const void* tma = nullptr;
-  const void* merge = nullptr;
+  const void* fn_inline = nullptr;    // the same kernels deriving unit records themselves
+  const void* tma_inline = nullptr;
+  const void* merge = nullptr;        // split lists of up to 4 per group
+  const void* merge_long = nullptr;   // longer split lists
   size_t (*smem)(int) = nullptr;
   size_t (*tma_fixed)(int) = nullptr;   // TMA variant: shared memory besides the ring
   int tma_stage_bytes = 0, tma_threads = 0, tma_blocks_per_sm = 0;
+  int merge_slices = 1;   // merge blocks per (token, KV head)
 };
 
 template <int D, int G>
 KernelInfo info() {
   KernelInfo k;
-  k.fn = reinterpret_cast<const void*>(&attn_kernel<D, G>);
-  k.tma = reinterpret_cast<const void*>(&attn_tma_kernel<D, G>);
+  k.fn = reinterpret_cast<const void*>(&attn_kernel<D, G, false>);
+  k.tma = reinterpret_cast<const void*>(&attn_tma_kernel<D, G, false>);
+  k.fn_inline = reinterpret_cast<const void*>(&attn_kernel<D, G, true>);
+  k.tma_inline = reinterpret_cast<const void*>(&attn_tma_kernel<D, G, true>);
   k.tma_fixed = &TmaCfg<D, G>::fixed_bytes;
   k.tma_stage_bytes = TmaCfg<D, G>::STAGE_BYTES;
   k.tma_threads = TmaCfg<D, G>::THREADS;
   k.tma_blocks_per_sm = TmaCfg<D, G>::BLOCKS_PER_SM;
-  k.merge = reinterpret_cast<const void*>(&merge_kernel<D, G>);
+  k.merge = reinterpret_cast<const void*>(&merge_kernel<D, G, 4>);
+  k.merge_long = reinterpret_cast<const void*>(&merge_kernel<D, G, 16>);
+  k.merge_slices = merge_slices_of<D, G>();
   k.smem = &Cfg<D, G>::smem_bytes;
   return k;
 }
@@ -1044,6 +1206,7 @@ struct bi_attention {
   // TMA page-box variant (page sizes 8, 16, 32, 64): ring depth, shared memory, grid bound
   bool tma = false;
   int nstage = 0, tma_ctas = 0;
+  int tma_ctas_inline = 0, max_ctas_inline = 0;   // grid bounds of the kernels deriving their units
   size_t tma_smem = 0;
   biattn::KernelInfo kern;
   uint32_t* d_status = nullptr;
@@ -1100,15 +1263,19 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
   // any handle of this kernel can need (split 1024).
   const size_t smem_cap = k.smem(1024);
   if (smem_cap > 232448) return BI_GEMM_ERR_UNSUPPORTED;
+  int per_sm_inline = 0;
   if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_cap)) != cudaSuccess ||
+      cudaFuncSetAttribute(k.fn_inline, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_cap)) != cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, biattn::kThreads, smem) != cudaSuccess ||
-      per_sm < 1) {
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_inline, k.fn_inline, biattn::kThreads, smem) !=
+          cudaSuccess ||
+      per_sm < 1 || per_sm_inline < 1) {
     cudaGetLastError();
     return BI_GEMM_ERR_CUDA;
   }
   // TMA variant: the deepest ring (up to 8 stages) with which its blocks per SM fit
   bool tma = false;
-  int nstage = 0, tma_per_sm = 0;
+  int nstage = 0, tma_per_sm = 0, tma_per_sm_inline = 0;
   size_t tma_smem = 0;
   if (page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64) {
     int sm_bytes = 0, reserved = 0, optin = 0;
@@ -1128,12 +1295,16 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
       // per kernel, shared by every handle of the head shape: the most a block may have
       if (cudaFuncSetAttribute(k.tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                optin - int(fa.sharedSizeBytes)) != cudaSuccess ||
+          cudaFuncSetAttribute(k.tma_inline, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               optin - int(fa.sharedSizeBytes)) != cudaSuccess ||
           cudaOccupancyMaxActiveBlocksPerMultiprocessor(&tma_per_sm, k.tma, k.tma_threads, tma_smem) !=
-              cudaSuccess) {
+              cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&tma_per_sm_inline, k.tma_inline, k.tma_threads,
+                                                        tma_smem) != cudaSuccess) {
         cudaGetLastError();
         return BI_GEMM_ERR_CUDA;
       }
-      tma = tma_per_sm >= 1;
+      tma = tma_per_sm >= 1 && tma_per_sm_inline >= 1;
     }
   }
   bi_attention* h = new (std::nothrow) bi_attention();
@@ -1142,6 +1313,8 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
   h->nstage = tma ? nstage : 0;
   h->tma_smem = tma_smem;
   h->tma_ctas = tma_per_sm * sms;
+  h->tma_ctas_inline = tma_per_sm_inline * sms;
+  h->max_ctas_inline = per_sm_inline * sms;
   h->Hq = int(num_q_heads);
   h->Hkv = int(num_kv_heads);
   h->D = int(head_dim);
@@ -1174,11 +1347,13 @@ BI_GEMM_API int bi_attention_workspace_size(bi_attention_t h, int64_t T, int64_t
 namespace {
 
 // bi_attention_run with the failure injection of the test controls (stall_block >= 0: that
-// block of the TMA kernel never issues its first load) and the limit of the ring waits.
+// block of the TMA kernel never issues its first load), the limit of the ring waits, and the
+// kernel choice (0: automatic; 1: the TMA page-box kernel where the handle has it; 2: the
+// row-copy kernel), which the test controls use to run both kernels on the same calls.
 int attention_run(bi_attention* h, const void* q, int64_t T, const int32_t* q_seq, const int32_t* q_pos,
                   const void* k_cache, const void* v_cache, int64_t num_pages, const int32_t* page_table,
                   int64_t num_seqs, int64_t max_pages, int64_t max_pos, void* o, void* stream, int32_t stall_block,
-                  uint64_t timeout_ns) {
+                  uint64_t timeout_ns, int32_t kernel_choice = 0) {
   if (!h || T < 0 || num_pages < 0 || num_seqs < 0 || max_pages < 0 || max_pos < 0) return BI_GEMM_ERR_INVALID_ARG;
   if (T == 0) return BI_GEMM_OK;
   if (T > (int64_t(1) << 24) || max_pos >= (int64_t(1) << 30) ||
@@ -1245,11 +1420,23 @@ int attention_run(bi_attention* h, const void* q, int64_t T, const int32_t* q_se
   // runs: both give the same bits.
   CUtensorMap tmk, tmv;
   const int64_t rows = num_pages * h->page_size;
-  const bool use_tma = h->tma && num_pages > 0 && rows + h->page_size < (int64_t(1) << 31) &&
+  // Small batches derive the unit records inside the attention kernel (same numbering), which
+  // saves the plan launch and its wait; larger ones read the plan's table.
+  p.inline_plan = T <= biattn::kInlinePlanMaxT ? 1 : 0;
+  // A call whose units fit in one round of the row-copy kernel's (more numerous, smaller) blocks
+  // but not in one round of the TMA kernel's runs the row-copy kernel: the second round of a few
+  // units would otherwise run alone at one block per SM.  The two kernels give the same bits.
+  const int64_t units_all = T * h->Hkv * int64_t(p.max_splits);
+  const bool one_round_rows = units_all > (p.inline_plan ? h->tma_ctas_inline : h->tma_ctas) &&
+                              units_all <= (p.inline_plan ? h->max_ctas_inline : h->max_ctas);
+  const bool want_tma = kernel_choice == 1 || (kernel_choice == 0 && !one_round_rows);
+  const bool use_tma = h->tma && want_tma && num_pages > 0 && rows + h->page_size < (int64_t(1) << 31) &&
                        biattn::encode_cache(&tmk, k_cache, rows, h->Hkv, h->D, h->page_size) &&
                        biattn::encode_cache(&tmv, v_cache, rows, h->Hkv, h->D, h->page_size);
-  biattn::plan_kernel<<<1, 1024, 0, st>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return BI_GEMM_ERR_CUDA;
+  if (!p.inline_plan) {
+    biattn::plan_kernel<<<1, 1024, 0, st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return BI_GEMM_ERR_CUDA;
+  }
   const int64_t units = T * h->Hkv * int64_t(p.max_splits);
   void* args[1] = {&p};
   void* targs[3] = {&tmk, &tmv, &p};
@@ -1263,21 +1450,24 @@ int attention_run(bi_attention* h, const void* q, int64_t T, const int32_t* q_se
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  const bool inl = p.inline_plan != 0;
   if (use_tma) {
-    cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, h->tma_ctas)));
+    cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, inl ? h->tma_ctas_inline : h->tma_ctas)));
     cfg.blockDim = dim3(h->kern.tma_threads);
     cfg.dynamicSmemBytes = h->tma_smem;
   } else {
-    cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, h->max_ctas)));
+    cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, inl ? h->max_ctas_inline : h->max_ctas)));
     cfg.blockDim = dim3(biattn::kThreads);
     cfg.dynamicSmemBytes = h->smem;
   }
-  cudaError_t e = cudaLaunchKernelExC(&cfg, use_tma ? h->kern.tma : h->kern.fn, use_tma ? targs : args);
+  const void* fn = use_tma ? (inl ? h->kern.tma_inline : h->kern.tma) : (inl ? h->kern.fn_inline : h->kern.fn);
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, use_tma ? targs : args);
   if (e == cudaSuccess) {
-    cfg.gridDim = dim3(unsigned(T * h->Hkv));
+    cfg.gridDim = dim3(unsigned(T * h->Hkv * h->kern.merge_slices));
     cfg.blockDim = dim3(biattn::kMergeThreads);
     cfg.dynamicSmemBytes = 0;
-    e = cudaLaunchKernelExC(&cfg, h->kern.merge, args);
+    // at most four splits per group: the instantiation with more resident blocks
+    e = cudaLaunchKernelExC(&cfg, (p.max_splits + 3) / 4 <= 4 ? h->kern.merge : h->kern.merge_long, args);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

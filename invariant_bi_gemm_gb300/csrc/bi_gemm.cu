@@ -22,6 +22,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <type_traits>
 
 #include "../../include/bi_gemm.h"
 #include "bi_gemm_kernel.cuh"
@@ -526,6 +527,112 @@ BI_GEMM_API int bi_gemm_workspace_size(bi_gemm_t h, int64_t M, uint64_t* bytes) 
   const int64_t tiles = shape_of(h, M).subtiles;
   *bytes = counters_bytes(tiles) + size_t(tiles) * h->split * kBM * h->kern.bn * sizeof(float);
   return BI_GEMM_OK;
+}
+
+// ------------------------------------------------------------------ gather + GEMM
+
+namespace bigemm {
+
+constexpr int kGatherMaxBlocks = 256;
+constexpr int kGatherThreads = 256;
+
+struct GatherParams {
+  const void* src[kGatherMaxBlocks];
+  int64_t off[kGatherMaxBlocks + 1];   // byte offset of each block in the destination
+  void* dst;
+};
+
+// Copy every block's bytes to its offset in dst: grid.y is the block, grid.x strides over its
+// bytes in 16-byte words (kWord = 16) or 4-byte words (kWord = 4; the MXFP8 scales, whose rows
+// are K/32 bytes).  A pure copy: HBM-bound, coalesced, no arithmetic.
+template <int kWord>
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(const __grid_constant__ GatherParams g) {
+  using W = typename std::conditional<kWord == 16, uint4, uint32_t>::type;
+  const int b = int(blockIdx.y);
+  const int64_t n = (g.off[b + 1] - g.off[b]) / kWord;
+  const W* src = static_cast<const W*>(g.src[b]);
+  W* dst = reinterpret_cast<W*>(static_cast<char*>(g.dst) + g.off[b]);
+  ptx::grid_dependency_wait();   // the blocks may be the previous kernel's output
+  for (int64_t i = int64_t(blockIdx.x) * kGatherThreads + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * kGatherThreads)
+    dst[i] = src[i];
+}
+
+}  // namespace bigemm
+
+namespace {
+
+int launch_gather(const void* const* srcs, const int64_t* bytes, int nb, void* dst, int word, int sms,
+                  cudaStream_t st) {
+  GatherParams g;
+  std::memset(&g, 0, sizeof(g));
+  int64_t mx = 0;
+  g.off[0] = 0;
+  for (int b = 0; b < nb; ++b) {
+    g.src[b] = srcs[b];
+    g.off[b + 1] = g.off[b] + bytes[b];
+    mx = std::max(mx, bytes[b]);
+  }
+  g.dst = dst;
+  if (mx == 0) return BI_GEMM_OK;
+  const int64_t words = mx / word;
+  const int64_t per_block = std::max<int64_t>(1, (int64_t(2) * sms + nb - 1) / nb);   // ~2 CTAs per SM
+  const unsigned gx = unsigned(std::min<int64_t>(per_block, (words + kGatherThreads - 1) / kGatherThreads));
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(std::max(1u, gx), unsigned(nb));
+  cfg.blockDim = dim3(kGatherThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[1] = {&g};
+  const void* fn = word == 16 ? reinterpret_cast<const void*>(&gather_kernel<16>)
+                              : reinterpret_cast<const void*>(&gather_kernel<4>);
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+    cudaGetLastError();
+    return BI_GEMM_ERR_CUDA;
+  }
+  return BI_GEMM_OK;
+}
+
+}  // namespace
+
+BI_GEMM_API int bi_gemm_run_gathered(bi_gemm_t h, const bi_gemm_block* blocks, int32_t nblocks, void* x_out,
+                                     uint8_t* sx_out, const void* W, const uint8_t* sw, void* y, void* stream) {
+  if (!h || !blocks || nblocks < 1 || nblocks > kGatherMaxBlocks) return BI_GEMM_ERR_INVALID_ARG;
+  const bool fp8 = h->dtype == BI_MXFP8E4M3_OUT_BF16;
+  const int64_t xrow = h->K * (fp8 ? 1 : 2), srow = h->K / 32;
+  int64_t M = 0;
+  const void* xs[kGatherMaxBlocks];
+  const void* ss[kGatherMaxBlocks];
+  int64_t xb[kGatherMaxBlocks], sb[kGatherMaxBlocks];
+  for (int b = 0; b < nblocks; ++b) {
+    const bi_gemm_block& k = blocks[b];
+    if (k.rows < 0 || (k.rows > 0 && !k.x) || (fp8 && k.rows > 0 && !k.sx) || (!fp8 && k.sx))
+      return BI_GEMM_ERR_INVALID_ARG;
+    if (!is_aligned(k.x, 16) || (fp8 && !is_aligned(k.sx, 4))) return BI_GEMM_ERR_ALIGNMENT;
+    M += k.rows;
+    if (M >= (int64_t(1) << 31)) return BI_GEMM_ERR_UNSUPPORTED;
+    xs[b] = k.x;
+    ss[b] = k.sx;
+    xb[b] = k.rows * xrow;
+    sb[b] = k.rows * srow;
+  }
+  if (fp8 && (!sx_out || !sw)) return BI_GEMM_ERR_INVALID_ARG;
+  if (!fp8 && (sx_out || sw)) return BI_GEMM_ERR_INVALID_ARG;
+  if (M == 0) return BI_GEMM_OK;
+  bi_gemm_scales sc{sx_out, sw};
+  int rc = validate_run(h, x_out, M, W, fp8 ? &sc : nullptr, y);
+  if (rc != BI_GEMM_OK) return rc;
+  std::lock_guard<std::mutex> lk(h->mu);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = launch_gather(xs, xb, nblocks, x_out, 16, h->num_sms, st);
+  if (rc == BI_GEMM_OK && fp8) rc = launch_gather(ss, sb, nblocks, sx_out, 4, h->num_sms, st);
+  if (rc != BI_GEMM_OK) return rc;
+  return launch(h, x_out, M, W, fp8 ? &sc : nullptr, y, st, 0, 0u);
 }
 
 BI_GEMM_API const char* bi_gemm_strerror(int code) {

@@ -18,7 +18,7 @@
 
 #include <cuda_bf16.h>
 
-#include "../../include/bi_gemm_controls.h"
+#include "../../tests/include/bi_gemm_controls.h"
 
 #define BI_CTL_API extern "C" __attribute__((visibility("default")))
 
@@ -180,5 +180,16 @@ BI_CTL_API int bi_ctl_attention_stall(bi_attention_t h, const void* q, int64_t T
   if (!h) return BI_GEMM_ERR_INVALID_ARG;
   if (!h->tma || timeout_ns == 0) return BI_GEMM_ERR_UNSUPPORTED;
   return attention_run(h, q, T, q_seq, q_pos, k_cache, v_cache, num_pages, page_table, num_seqs, max_pages, max_pos, o,
-                       stream, 0, timeout_ns);
+                       stream, 0, timeout_ns, 1);
+}
+
+BI_CTL_API int bi_ctl_attention_run_kernel(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,
+                                           const int32_t* q_pos, const void* k_cache, const void* v_cache,
+                                           int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                                           int64_t max_pages, int64_t max_pos, void* o, int32_t kernel,
+                                           void* stream) {
+  if (!h || kernel < 1 || kernel > 2) return BI_GEMM_ERR_INVALID_ARG;
+  if (kernel == 1 && !h->tma) return BI_GEMM_ERR_UNSUPPORTED;
+  return attention_run(h, q, T, q_seq, q_pos, k_cache, v_cache, num_pages, page_table, num_seqs, max_pages, max_pos, o,
+                       stream, -1, biattn::kTimeoutNs, kernel);
 }

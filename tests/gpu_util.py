@@ -48,6 +48,28 @@ def byte_diffs(a: np.ndarray, b: np.ndarray) -> int:
     return int(np.count_nonzero(a != b))
 
 
+def oracle_rows(fn, rows, chunks=None):
+    """Run an oracle call `fn(rows) -> (y, acc, sabs)` over `rows` split across host threads (the
+    C oracle releases the interpreter lock; rows are independent, so the result is the same as one
+    call) and stack the pieces in the order of `rows`."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    rows = np.asarray(list(rows), dtype=np.int64)
+    n = chunks or max(1, min(len(rows), os.cpu_count() or 1))
+    parts = [np.arange(i, len(rows), n) for i in range(n)]
+    parts = [p for p in parts if p.size]
+    with ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        outs = list(ex.map(lambda p: fn(rows[p]), parts))
+    res = []
+    for k in range(3):
+        first = outs[0][k]
+        full = np.empty((len(rows),) + first.shape[1:], dtype=first.dtype)
+        for p, o in zip(parts, outs):
+            full[p] = o[k]
+        res.append(full)
+    return tuple(res)
+
+
 def check_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, sabs: np.ndarray, tol: float, what: str):
     """|y - y_ref| <= tol * S_abs elementwise; returns the max ratio for reporting."""
     bad, ratio = oracle.tolerance_violations(to_f64(y_gpu), to_f64(y_ref), sabs, tol)
@@ -77,7 +99,7 @@ def bi_check(run, rows_a: torch.Tensor, rows_b: torch.Tensor, content: torch.Ten
 
 
 class Controls:
-    """ctypes view of the test-only libbi_gemm_controls.so (include/bi_gemm_controls.h)."""
+    """ctypes view of the test-only libbi_gemm_controls.so (tests/include/bi_gemm_controls.h)."""
 
     def __init__(self):
         L = ctypes.CDLL(bgbuild.lib_path("libbi_gemm_controls.so"))
@@ -97,10 +119,12 @@ class Controls:
         L.bi_ctl_attention_run.argtypes = [P, P, I64, P, P, P, P, I64, P, I64, I64, I64, P, P]
         L.bi_ctl_attention_get_device_error.argtypes = [P, P]
         L.bi_ctl_attention_destroy.argtypes = [P]
+        L.bi_ctl_attention_run_kernel.argtypes = [P, P, I64, P, P, P, P, I64, P, I64, I64, I64, P, ctypes.c_int32, P]
         for n in ("bi_ctl_create", "bi_ctl_destroy", "bi_ctl_get_device_error", "bi_ctl_run",
                   "bi_ctl_msplit_count", "bi_ctl_run_msplit", "bi_ctl_run_smallm_fork", "bi_ctl_run_stall",
                   "bi_ctl_run_skip_arrival", "bi_ctl_rmsnorm_f32", "bi_ctl_attention_stall", "bi_ctl_attention_create",
-                  "bi_ctl_attention_run", "bi_ctl_attention_get_device_error", "bi_ctl_attention_destroy"):
+                  "bi_ctl_attention_run", "bi_ctl_attention_get_device_error", "bi_ctl_attention_destroy",
+                  "bi_ctl_attention_run_kernel"):
             getattr(L, n).restype = I32
         self.L = L
 

@@ -1,5 +1,6 @@
 /*
- * bi_gemm_controls.h — TEST-ONLY C ABI of libbi_gemm_controls.so.
+ * bi_gemm_controls.h — TEST-ONLY C ABI of libbi_gemm_controls.so (kept beside the tests, outside
+ * the product's include/).
  *
  * Deliberately batch-variant negative controls, for proving that the batch-invariance
  * harness can fail, and a failure-injection hook for the bounded in-kernel waits.  The
@@ -16,8 +17,8 @@
 
 #include <stdint.h>
 
-#include "bi_attention.h"
-#include "bi_gemm.h"
+#include "../../include/bi_attention.h"
+#include "../../include/bi_gemm.h"
 
 #ifdef __cplusplus
 extern "C" {
@@ -91,6 +92,14 @@ int bi_ctl_attention_stall(bi_attention_t h, const void* q, int64_t T, const int
                            int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
                            int64_t max_pages, int64_t max_pos, void* o, uint64_t timeout_ns,
                            void* stream);
+
+/* bi_attention_run with the kernel pinned (kernel = 1: the TMA page-box kernel, for a handle
+ * whose config has tma_pages = 1, else BI_GEMM_ERR_UNSUPPORTED; kernel = 2: the row-copy
+ * kernel), so that tests can run both kernels on the same calls whichever the product picks. */
+int bi_ctl_attention_run_kernel(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,
+                                const int32_t* q_pos, const void* k_cache, const void* v_cache,
+                                int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                                int64_t max_pages, int64_t max_pos, void* o, int32_t kernel, void* stream);
 
 #ifdef __cplusplus
 }

@@ -7,7 +7,7 @@ import pytest
 
 import inputgen as ig
 import oracle
-from gpu_util import check_tolerance, dev_bf16, host_bits
+from gpu_util import check_tolerance, dev_bf16, host_bits, oracle_rows
 from invariant_bi_gemm_gb300 import BiGemm
 
 pytestmark = pytest.mark.gpu
@@ -37,10 +37,30 @@ def test_first_row_alone_equals_first_row_of_full(setup):
     assert np.array_equal(y_last.view(np.uint32), y_full[-1:].view(np.uint32))
 
 
+def sample_rows():
+    """64 rows of the M = 2048 output: tile and batch boundaries, {0, mid, last}, seeded rows."""
+    rows = {0, 1, 2, 63, 64, 127, 128, 255, 256, 1023, 1024, 2046, 2047}
+    rng = np.random.default_rng(20240611)
+    while len(rows) < 64:
+        rows.add(int(rng.integers(0, B_ROWS)))
+    return sorted(rows)
+
+
 def test_parity_sampled_rows(setup):
+    """64 sampled rows of the full M = 2048 launch, every column, against the oracle."""
     g, a, b, ad, bd = setup
-    rows = [0, 1, 2, 127, 128, 1023, 1024, 2046, 2047]
-    y_ref, _, sabs = oracle.gemm_bf16(a, b, "f32", rows=rows)
+    rows = sample_rows()
+    y_ref, _, sabs = oracle_rows(lambda r: oracle.gemm_bf16(a, b, "f32", rows=r), rows)
     y = host_bits(g(ad, bd))[rows]
     worst = check_tolerance(y, y_ref, sabs, oracle.TOL_F32, "linspace")
     print(f"linspace fp32 max |y-y_ref|/S_abs = {worst:.3g}")
+
+
+@pytest.mark.parametrize("M", [1, 17, 64])
+def test_parity_every_element_small_m(setup, M):
+    """Every element of the launches with M <= 64 rows against the oracle."""
+    g, a, b, ad, bd = setup
+    y_ref, _, sabs = oracle_rows(lambda r: oracle.gemm_bf16(a[:M], b, "f32", rows=r), list(range(M)))
+    y = host_bits(g(ad[:M].contiguous(), bd))
+    worst = check_tolerance(y, y_ref, sabs, oracle.TOL_F32, f"linspace M={M}")
+    print(f"linspace M={M} fp32 max |y-y_ref|/S_abs = {worst:.3g}")

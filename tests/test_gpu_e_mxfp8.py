@@ -14,7 +14,7 @@ import torch
 
 import inputgen as ig
 import oracle
-from gpu_util import byte_diffs, check_tolerance, dev_u8, host_bits
+from gpu_util import byte_diffs, check_tolerance, dev_u8, host_bits, oracle_rows
 from invariant_bi_gemm_gb300 import BiGemm
 
 pytestmark = pytest.mark.gpu
@@ -94,8 +94,14 @@ def test_mxfp8_llm_shape():
     for M in (1, 17, 129, 1000):
         yM = g(xd[:M], wd, sx=sxd[:M], sw=swd)
         assert torch.equal(yM.view(torch.int16), y_full[:M].view(torch.int16)), M
-    rows = [0, 1, 127, 128, 1023, 2047]
-    y_ref, _, sabs = oracle.gemm_mxfp8(x, sx, w, sw, rows=rows)
+    # every element of rows 0..63 (the M <= 64 launches are bitwise those rows), and 64 sampled rows
+    # of the rest: tile and batch boundaries, {mid, last} and seeded rows
+    rows = set(range(64)) | {127, 128, 255, 256, 511, 1023, 1024, 2047}
+    rng = np.random.default_rng(20240612)
+    while len(rows) < 128:
+        rows.add(int(rng.integers(64, MM)))
+    rows = sorted(rows)
+    y_ref, _, sabs = oracle_rows(lambda r: oracle.gemm_mxfp8(x, sx, w, sw, rows=r), rows)
     check_tolerance(host_bits(y_full)[rows], y_ref, sabs, oracle.TOL_BF16, "MXFP8 LLM shape")
     g.close()
 

@@ -228,23 +228,67 @@ def test_empty_batch_and_misaligned_pointers():
     attn.close()
 
 
+def run_pinned(bt, Hq, Hkv, D, page, kernel, split=512):
+    """bt on a handle of the test-only controls library with the kernel pinned (1: TMA page boxes,
+    2: row copies), whichever the product would pick for the call."""
+    from gpu_util import Controls
+    L = Controls().L
+    P, V = ctypes.c_void_p, ctypes.c_void_p
+    h = P()
+    assert L.bi_ctl_attention_create(ctypes.byref(h), Hq, Hkv, D, page, ctypes.c_float(float(D) ** -0.5), split) == 0
+    d = {k: torch.from_numpy(getattr(bt, k)).cuda() for k in ("q_seq", "q_pos", "table")}
+    bf = {k: torch.from_numpy(getattr(bt, k).view(np.int16)).cuda().view(torch.bfloat16) for k in ("q", "kc", "vc")}
+    o = torch.full_like(bf["q"], float("nan"))
+    rc = L.bi_ctl_attention_run_kernel(h, V(bf["q"].data_ptr()), bf["q"].shape[0], V(d["q_seq"].data_ptr()),
+                                       V(d["q_pos"].data_ptr()), V(bf["kc"].data_ptr()), V(bf["vc"].data_ptr()),
+                                       bf["kc"].shape[0], V(d["table"].data_ptr()), d["table"].shape[0],
+                                       d["table"].shape[1], bt.max_pos, V(o.data_ptr()), kernel, stream_ptr())
+    assert rc == 0, rc
+    assert L.bi_ctl_attention_get_device_error(h, stream_ptr()) == 0
+    assert L.bi_ctl_attention_destroy(h) == 0
+    return o.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
 def test_tma_page_boxes_and_row_copies_give_the_same_bits():
-    """Page sizes 8, 16, 32 and 64 run the kernel whose producer warp loads pages as TMA boxes;
-    other page sizes the kernel whose threads copy rows.  Their arithmetic is the same, so the
-    same requests give the same bits whichever runs, including ragged last stages (lengths that
-    end inside a page and inside a 16-position step) and single-key splits."""
+    """Page sizes 8, 16, 32 and 64 can run the kernel whose producer warp loads pages as TMA
+    boxes; every page size the kernel whose threads copy rows.  Their arithmetic is the same, so
+    the same requests give the same bits whichever runs (each kernel pinned through the test
+    controls), including ragged last stages (lengths that end inside a page and inside a
+    16-position step) and single-key splits; the product's own choice gives them too."""
     Hq, Hkv, D = 32, 8, 128
     lens = [1, 15, 17, 63, 64, 65, 200, 511, 512, 513, 1000, 2049]
     outs, flags = {}, {}
     for page in (8, 16, 32, 64, 12, 1):
         attn = BiAttention(Hq, Hkv, D, page, split_size=512)
         flags[page] = attn.config["tma_pages"]
-        outs[page] = decode_batch(lens, Hq, Hkv, D, page, page_seed=page).run(attn)
+        bt = decode_batch(lens, Hq, Hkv, D, page, page_seed=page)
+        outs[page] = bt.run(attn)
         assert attn.device_error() == 0
         attn.close()
+        if flags[page]:
+            assert byte_diffs(run_pinned(bt, Hq, Hkv, D, page, 1), outs[page]) == 0, ("TMA", page)
+        assert byte_diffs(run_pinned(bt, Hq, Hkv, D, page, 2), outs[page]) == 0, ("rows", page)
     assert flags == {8: 1, 16: 1, 32: 1, 64: 1, 12: 0, 1: 0}
     for page in (16, 32, 64, 12, 1):
         assert byte_diffs(outs[page], outs[8]) == 0, page
+
+
+@pytest.mark.parametrize("lens", [[32768], [4096] * 8, [28672], [3000] * 20])
+def test_kernel_choice_changes_no_bit(lens):
+    """A call whose units fit in one round of the row-copy kernel's blocks but not of the TMA
+    kernel's runs the row-copy kernel (batch 1 x 32768 and 8 x 4096: 512 units); smaller and
+    larger calls run the TMA kernel.  Whichever the product picks, the bits are those of both
+    kernels pinned, and the request alone (batch 1) gives the same bits as inside its batch."""
+    Hq, Hkv, D = 32, 8, 128
+    bt = decode_batch(lens, Hq, Hkv, D, 16)
+    attn = BiAttention(Hq, Hkv, D, 16)
+    auto = bt.run(attn)
+    assert attn.device_error() == 0
+    assert byte_diffs(run_pinned(bt, Hq, Hkv, D, 16, 1), auto) == 0
+    assert byte_diffs(run_pinned(bt, Hq, Hkv, D, 16, 2), auto) == 0
+    one = decode_batch(lens[:1], Hq, Hkv, D, 16).run(attn)
+    assert byte_diffs(one, auto[:1]) == 0
+    attn.close()
 
 
 @pytest.mark.parametrize("D,G", [(64, 8), (64, 1), (128, 2)])

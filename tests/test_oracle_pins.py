@@ -397,3 +397,16 @@ def test_bad_arguments_rejected():
     w = ig.normal_bf16(2, 4, 2)
     with pytest.raises(ValueError):
         oracle.gemm_bf16(x, w, "bf16", rows=[2])
+
+
+def test_oracle_rows_helper_matches_one_call():
+    """The GPU tests spread large oracle calls over host threads (tests/gpu_util.py:oracle_rows);
+    the pieces must come back in the order of the requested rows, equal to one call."""
+    import gpu_util
+    x = ig.normal_bf16(ig.SEED_X, 40, 64)
+    w = ig.normal_bf16(ig.SEED_W, 64, 24)
+    rows = [5, 0, 39, 12, 7, 3, 5]
+    one = oracle.gemm_bf16(x, w, "f32", rows=rows)
+    for chunks in (1, 3, 7):
+        got = gpu_util.oracle_rows(lambda r: oracle.gemm_bf16(x, w, "f32", rows=r), rows, chunks=chunks)
+        assert all(np.array_equal(a, b) for a, b in zip(one, got))
