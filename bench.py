@@ -42,7 +42,12 @@ STATIC_W = True
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of each launch of the sweep, from one
 # ncu capture of `python bench.py --steps 1 --warmup 3 --no-paths --no-cpu` (the command and the
 # figures are in profiles/ncu_bf16_gemm_llm_sweep.md), for the kernel sources of the given hash.
-TRAFFIC = {"source_sha256_16": None, "bytes_per_launch": {}}
+TRAFFIC = {"source_sha256_16": "7eb081cfb2d3ae24", "bytes_per_launch": {
+    1: 120480000, 7: 117983232, 8: 117764096, 15: 117652992,
+    16: 117676544, 17: 117715712, 63: 118142720, 64: 118158592,
+    65: 118145024, 128: 118604288, 129: 118596096, 192: 119118848,
+    193: 119199232, 256: 119720192, 512: 123275520, 1024: 141131520,
+    2048: 175838464, 4096: 280269824, 8192: 731410176}}
 
 
 def flops(M, K=K_DIM, N=N_DIM):
@@ -567,10 +572,30 @@ def measure_e2e(g, W_np, X_np, args, dev, world):
     h2d_bytes = 2 * K_DIM * N_DIM + sum(2 * M * K_DIM for M in M_SWEEP)
     d2h_bytes = sum(2 * M * N_DIM for M in M_SWEEP)
     fl = sum(flops(M) for M in M_SWEEP) * steps * world
+    # the host link alone: the same copies per step, both directions at once, without the GEMMs
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(comp)
+    h2d.wait_event(c0)
+    d2h.wait_event(c0)
+    for s in range(steps):
+        with torch.cuda.stream(h2d):
+            Wd[s % 2].copy_(Wh, non_blocking=True)
+            Xd.copy_(Xh, non_blocking=True)
+        with torch.cuda.stream(d2h):
+            Yh.copy_(Yd, non_blocking=True)
+    comp.wait_stream(h2d)
+    comp.wait_stream(d2h)
+    c1.record(comp)
+    torch.cuda.synchronize()
+    link_ms = c0.elapsed_time(c1) / steps
     return {"value": round(fl / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_bytes,
             "d2h_bytes_per_step": d2h_bytes, "steps": steps, "ms_per_step": round(ms / steps, 3),
+            "copies_only_ms_per_step": round(link_ms, 3),
+            "copies_only_gbs": round((h2d_bytes + d2h_bytes) / (link_ms / 1e3) / 1e9, 1),
             "how": "pinned host buffers; host-to-device copies, GEMMs and device-to-host copies on three "
-                   "streams ordered by events (copies overlap GEMMs of other launches)"}
+                   "streams ordered by events (copies overlap GEMMs of other launches); copies_only: the "
+                   "same bytes copied both ways at once without the GEMMs, the host link's own time"}
 
 
 def measure_other_paths(dev, peaks):
