@@ -183,6 +183,23 @@ def test_long_context_sampled():
     attn.close()
 
 
+def test_merge_of_long_split_lists():
+    """Contexts past 64 splits (the merge's four groups then hold more than 16 splits each and are
+    summed over several batches of loads, in the same order): every element against the oracle,
+    and the long request's bits unchanged alone and beside a short one."""
+    Hq, Hkv, D = 32, 8, 128
+    lens = [40000, 33000, 100]
+    bt = decode_batch(lens, Hq, Hkv, D, 16)
+    attn = BiAttention(Hq, Hkv, D, 16)
+    o = bt.run(attn)
+    assert attn.device_error() == 0
+    _, v, a, e = bt.oracle(np.float32(attn.scale))
+    within(o, v, a, e, D, bt.q_pos + 1)
+    alone = decode_batch(lens[:1], Hq, Hkv, D, 16).run(attn)
+    assert byte_diffs(alone, o[:1]) == 0
+    attn.close()
+
+
 def test_repeat_runs_identical():
     bt = decode_batch([300, 5000, 17, 1024], 32, 8, 128, 16)
     attn = BiAttention(32, 8, 128, 16)
