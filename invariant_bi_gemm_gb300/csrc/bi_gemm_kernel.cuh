@@ -142,7 +142,7 @@ struct KCfg {
   static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
   // full, empty, accumulator full / empty, drain, epilogue; MXFP8 adds per stage the peer's
   // scales-ready barrier and per scale warp a drain barrier for its scale copies
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 2 + (kFp8 ? STAGES + SCALE_WARPS : 0);
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 2 + (kFp8 ? 2 * STAGES + SCALE_WARPS : 0);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   // epilogue staging for TMA stores: per epilogue warp, one or two 32 x 32 output blocks
   static constexpr int OUT_BYTES = kOutF32 ? 4 : 2;
@@ -280,6 +280,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   auto sfpeer_bar = [&](int s) { return epi_bar + 8u + 8u * s; };
   // MXFP8: completion of a scale warp's last scale copies
   auto sfdrain_bar = [&](int w) { return epi_bar + 8u + 8u * (C::STAGES + w); };
+  // MXFP8: a stage's scale slot has been copied into TMEM (in both CTAs of a pair) and may be
+  // refilled
+  auto sfdone_bar = [&](int s) { return epi_bar + 8u + 8u * (C::STAGES + C::SCALE_WARPS + s); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_slot = misc + 0;
   volatile uint32_t* abort_flag = misc + 1;
@@ -313,6 +316,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if constexpr (C::kFp8) {
       for (int s = 0; s < C::STAGES; ++s) ptx::mbar_init(sfpeer_bar(s), 1u);
       for (int w = 0; w < C::SCALE_WARPS; ++w) ptx::mbar_init(sfdrain_bar(w), 1u);
+      for (int s = 0; s < C::STAGES; ++s) ptx::mbar_init(sfdone_bar(s), 1u);
     }
     *abort_flag = 0u;
     *last_flag = 0u;
@@ -557,11 +561,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // byte (r % 32) * 16 + (r / 32) * 4 + kblk.  One 512-byte block for this CTA's 128 rows
         // of x, one per 128 columns of the tile's W columns (all BN of them, on a pair too).
         // This CTA's k-block items are numbered it = 0, 1, ... in pipeline order; scale warp j
-        // fills items j, j + SCALE_WARPS, ...: once the item's stage is free it copies the scales
-        // into the stage (cp.async) and rearranges them there.
-        // On a pair the peer's warp publishes its stage to the leader (sfpeer_bar); the leader's
-        // warp then issues the tcgen05.cp of both CTAs' scales and commits them to the stage's
-        // full barrier, so the MMA issuer finds the scales in TMEM and issues only MMAs.
+        // fills items j, j + SCALE_WARPS, ...: once the stage's scale slot has been copied into
+        // TMEM for the previous item (sfdone_bar), it copies the item's scales into the slot
+        // (cp.async) and rearranges them there, ahead of the MMAs.
+        // On a pair the peer's warp publishes its slot to the leader (sfpeer_bar); the leader's
+        // warp waits until the stage is free (its MMAs done), issues the tcgen05.cp of both CTAs'
+        // scales and commits them to the stage's full barrier and to both CTAs' sfdone_bar, so
+        // the MMA issuer finds the scales in TMEM and issues only MMAs.
         const int sw_id = warp - 2;
         const int KB32 = p.K / 32;
         int u = group, kb = 0, kb_end = 0, row_base = 0, col_base = 0;
@@ -592,7 +598,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         while (valid) {
           const int stage = it % C::STAGES;
           const uint32_t phase = uint32_t(it / C::STAGES) & 1u;
-          if (!warp_wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutScales)) break;
+          // The slot may be refilled once its previous scales are in TMEM: the loads and the
+          // rearrangement below run up to STAGES items ahead of the MMAs; only the copy into
+          // the stage's TMEM columns waits for the stage to be free.
+          if (!warp_wait_phase(sfdone_bar(stage), phase ^ 1u, sc, kErrTimeoutScales)) break;
           const uint32_t sf_addr = sbase + C::OFF_SF + stage * C::SF_BYTES;
           const uint32_t sfb_addr = sf_addr + C::SFA_BYTES;
           // x: this k-block's four scales of a row (one 32-bit word) go straight to the row's place
@@ -657,8 +666,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             } else {
               // leader (or single CTA): once the peer's scales are in place too, copy both CTAs'
               // scales into TMEM and count the copies' completion on the stage's full barrier
-              bool ready = true;
-              if constexpr (kPair) ready = wait_phase<Wait::kCluster>(sfpeer_bar(stage), phase, sc, kErrTimeoutScales);
+              bool ready = wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutScales);
+              if constexpr (kPair)
+                ready = ready && wait_phase<Wait::kCluster>(sfpeer_bar(stage), phase, sc, kErrTimeoutScales);
               if (ready) {
                 ptx::tc_fence_after();
                 const uint32_t sfa_t = tmem_base + uint32_t(C::SF_TMEM_COL0 + 16 * stage);
@@ -676,10 +686,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                   else
                     ptx::tc_cp_32x128b_x4(sfb_t + 4u * b, sfb_d);
                 }
-                if constexpr (kPair)
+                if constexpr (kPair) {
                   ptx::tc_commit_pair_mc(full_bar(stage), 0x1);
-                else
+                  ptx::tc_commit_pair_mc(sfdone_bar(stage), 0x3);   // both CTAs' slots are free
+                } else {
                   ptx::tc_commit(full_bar(stage));
+                  ptx::tc_commit(sfdone_bar(stage));
+                }
                 copied = true;
               }
               ok = ready;
