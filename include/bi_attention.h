@@ -82,9 +82,10 @@ int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, int64_t num_kv
  *
  * Two attention kernels, with the same arithmetic and the same bits: for page sizes 8, 16, 32
  * and 64 (a 64-position stage is whole pages) a producer warp loads every page's rows of a KV
- * head as 3-D TMA boxes into a ring that runs ahead across units, and four warps compute; for
- * other page sizes (or a cache of 2^31 rows or more) every thread copies 16-byte row chunks
- * with cp.async.  The waits of the TMA kernel on its ring are bounded (2 s): past the limit the
+ * head as 3-D TMA boxes into a ring that runs ahead across units, and four warps compute (three
+ * blocks per SM with a deeper ring, or, for a call that fits one round of four blocks per SM but
+ * not of three, four blocks with a shallower ring); for other page sizes (or a cache of 2^31 rows
+ * or more) every thread copies 16-byte row chunks with cp.async.  The waits of the TMA kernel on its ring are bounded (2 s): past the limit the
  * block stops, its output is undefined and bi_attention_get_device_error reports
  * BI_GEMM_ERR_TIMEOUT. */
 int bi_attention_run(bi_attention_t h, const void* q, int64_t T, const int32_t* q_seq,

@@ -650,8 +650,11 @@ __device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, const P
   return true;
 }
 
-template <int D, int G, bool kInline>
-__global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, TmaCfg<D, G>::BLOCKS_PER_SM)
+// kBlocksPerSm: the resident blocks per SM the registers are budgeted for: 3, with the ring sized
+// for them, or 4, with the ring that four blocks leave room for (two stages at a head dimension of
+// 128), so that a call of up to four units per SM runs in one round.
+template <int D, int G, bool kInline, int kBlocksPerSm>
+__global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, kBlocksPerSm)
     attn_tma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Params p) {
   using C = Cfg<D, G>;
   using TC = TmaCfg<D, G>;
@@ -1122,6 +1125,8 @@ struct KernelInfo {
   const void* tma = nullptr;
   const void* fn_inline = nullptr;    // the same kernels deriving unit records themselves
   const void* tma_inline = nullptr;
+  const void* tma4 = nullptr;         // the TMA kernels with registers for four blocks per SM
+  const void* tma4_inline = nullptr;
   const void* merge = nullptr;        // split lists of up to 4 per group
   const void* merge_long = nullptr;   // longer split lists
   size_t (*smem)(int) = nullptr;
@@ -1134,9 +1139,11 @@ template <int D, int G>
 KernelInfo info() {
   KernelInfo k;
   k.fn = reinterpret_cast<const void*>(&attn_kernel<D, G, false>);
-  k.tma = reinterpret_cast<const void*>(&attn_tma_kernel<D, G, false>);
+  k.tma = reinterpret_cast<const void*>(&attn_tma_kernel<D, G, false, TmaCfg<D, G>::BLOCKS_PER_SM>);
   k.fn_inline = reinterpret_cast<const void*>(&attn_kernel<D, G, true>);
-  k.tma_inline = reinterpret_cast<const void*>(&attn_tma_kernel<D, G, true>);
+  k.tma_inline = reinterpret_cast<const void*>(&attn_tma_kernel<D, G, true, TmaCfg<D, G>::BLOCKS_PER_SM>);
+  k.tma4 = reinterpret_cast<const void*>(&attn_tma_kernel<D, G, false, 4>);
+  k.tma4_inline = reinterpret_cast<const void*>(&attn_tma_kernel<D, G, true, 4>);
   k.tma_fixed = &TmaCfg<D, G>::fixed_bytes;
   k.tma_stage_bytes = TmaCfg<D, G>::STAGE_BYTES;
   k.tma_threads = TmaCfg<D, G>::THREADS;
@@ -1208,6 +1215,11 @@ struct bi_attention {
   int nstage = 0, tma_ctas = 0;
   int tma_ctas_inline = 0, max_ctas_inline = 0;   // grid bounds of the kernels deriving their units
   size_t tma_smem = 0;
+  // the TMA kernel with registers for four blocks per SM (a shallower ring), for calls that fit
+  // in one round of its blocks but not of the three-block kernel's
+  bool tma4 = false;
+  int nstage4 = 0, tma4_ctas = 0, tma4_ctas_inline = 0;
+  size_t tma4_smem = 0;
   biattn::KernelInfo kern;
   uint32_t* d_status = nullptr;
   void* ws = nullptr;
@@ -1276,7 +1288,8 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
   // TMA variant: the deepest ring (up to 8 stages) with which its blocks per SM fit
   bool tma = false;
   int nstage = 0, tma_per_sm = 0, tma_per_sm_inline = 0;
-  size_t tma_smem = 0;
+  int nstage4 = 0, tma4_per_sm = 0, tma4_per_sm_inline = 0;
+  size_t tma_smem = 0, tma4_smem = 0;
   if (page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64) {
     int sm_bytes = 0, reserved = 0, optin = 0;
     cudaFuncAttributes fa;
@@ -1306,6 +1319,28 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
       }
       tma = tma_per_sm >= 1 && tma_per_sm_inline >= 1;
     }
+    // the same kernel with registers for four blocks per SM and the ring that four leave room for
+    cudaFuncAttributes fa4;
+    if (tma && cudaFuncGetAttributes(&fa4, k.tma4) == cudaSuccess) {
+      const int64_t budget4 = int64_t(sm_bytes) / 4 - reserved - int64_t(fa4.sharedSizeBytes) -
+                              int64_t(k.tma_fixed(int(split)));
+      nstage4 = int(std::min<int64_t>(biattn::kTmaMaxStages, budget4 / (k.tma_stage_bytes + 16)));
+      if (nstage4 >= 2) {
+        tma4_smem = k.tma_fixed(int(split)) + size_t(nstage4) * (k.tma_stage_bytes + 16);
+        if (cudaFuncSetAttribute(k.tma4, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - int(fa4.sharedSizeBytes)) != cudaSuccess ||
+            cudaFuncSetAttribute(k.tma4_inline, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - int(fa4.sharedSizeBytes)) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&tma4_per_sm, k.tma4, k.tma_threads, tma4_smem) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&tma4_per_sm_inline, k.tma4_inline, k.tma_threads,
+                                                          tma4_smem) != cudaSuccess) {
+          cudaGetLastError();
+          return BI_GEMM_ERR_CUDA;
+        }
+      }
+    }
+    cudaGetLastError();
   }
   bi_attention* h = new (std::nothrow) bi_attention();
   if (!h) return BI_GEMM_ERR_OOM;
@@ -1315,6 +1350,12 @@ BI_GEMM_API int bi_attention_create(bi_attention_t* out, int64_t num_q_heads, in
   h->tma_ctas = tma_per_sm * sms;
   h->tma_ctas_inline = tma_per_sm_inline * sms;
   h->max_ctas_inline = per_sm_inline * sms;
+  // the four-block kernel only where it fits more blocks per SM than the three-block one
+  h->tma4 = tma && nstage4 >= 2 && tma4_per_sm > tma_per_sm && tma4_per_sm_inline > tma_per_sm_inline;
+  h->nstage4 = h->tma4 ? nstage4 : 0;
+  h->tma4_smem = tma4_smem;
+  h->tma4_ctas = h->tma4 ? tma4_per_sm * sms : 0;
+  h->tma4_ctas_inline = h->tma4 ? tma4_per_sm_inline * sms : 0;
   h->Hq = int(num_q_heads);
   h->Hkv = int(num_kv_heads);
   h->D = int(head_dim);
@@ -1424,11 +1465,16 @@ int attention_run(bi_attention* h, const void* q, int64_t T, const int32_t* q_se
   // saves the plan launch and its wait; larger ones read the plan's table.
   p.inline_plan = T <= biattn::kInlinePlanMaxT ? 1 : 0;
   // A call whose units fit in one round of the row-copy kernel's (more numerous, smaller) blocks
-  // but not in one round of the TMA kernel's runs the row-copy kernel: the second round of a few
-  // units would otherwise run alone at one block per SM.  The two kernels give the same bits.
+  // but not in one round of either TMA kernel's runs the row-copy kernel: the second round of a
+  // few units would otherwise run alone at one block per SM.  A call that fits in one round of
+  // the four-block TMA kernel but not of the three-block one runs the four-block kernel (its
+  // shallower ring costs less than a second round).  All give the same bits.
   const int64_t units_all = T * h->Hkv * int64_t(p.max_splits);
-  const bool one_round_rows = units_all > (p.inline_plan ? h->tma_ctas_inline : h->tma_ctas) &&
-                              units_all <= (p.inline_plan ? h->max_ctas_inline : h->max_ctas);
+  const bool inl = p.inline_plan != 0;
+  const int64_t tma3_slots = inl ? h->tma_ctas_inline : h->tma_ctas;
+  const int64_t tma4_slots = h->tma4 ? (inl ? h->tma4_ctas_inline : h->tma4_ctas) : 0;
+  const bool one_round_rows = units_all > std::max(tma3_slots, tma4_slots) &&
+                              units_all <= (inl ? h->max_ctas_inline : h->max_ctas);
   const bool want_tma = kernel_choice == 1 || (kernel_choice == 0 && !one_round_rows);
   const bool use_tma = h->tma && want_tma && num_pages > 0 && rows + h->page_size < (int64_t(1) << 31) &&
                        biattn::encode_cache(&tmk, k_cache, rows, h->Hkv, h->D, h->page_size) &&
@@ -1450,17 +1496,20 @@ int attention_run(bi_attention* h, const void* q, int64_t T, const int32_t* q_se
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const bool inl = p.inline_plan != 0;
+  const bool use_tma4 = use_tma && units_all > tma3_slots && units_all <= tma4_slots;
   if (use_tma) {
-    cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, inl ? h->tma_ctas_inline : h->tma_ctas)));
+    cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, use_tma4 ? tma4_slots : tma3_slots)));
     cfg.blockDim = dim3(h->kern.tma_threads);
-    cfg.dynamicSmemBytes = h->tma_smem;
+    cfg.dynamicSmemBytes = use_tma4 ? h->tma4_smem : h->tma_smem;
+    p.nstage = use_tma4 ? h->nstage4 : h->nstage;
   } else {
     cfg.gridDim = dim3(unsigned(std::min<int64_t>(units, inl ? h->max_ctas_inline : h->max_ctas)));
     cfg.blockDim = dim3(biattn::kThreads);
     cfg.dynamicSmemBytes = h->smem;
   }
-  const void* fn = use_tma ? (inl ? h->kern.tma_inline : h->kern.tma) : (inl ? h->kern.fn_inline : h->kern.fn);
+  const void* fn = use_tma ? (use_tma4 ? (inl ? h->kern.tma4_inline : h->kern.tma4)
+                                       : (inl ? h->kern.tma_inline : h->kern.tma))
+                           : (inl ? h->kern.fn_inline : h->kern.fn);
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, use_tma ? targs : args);
   if (e == cudaSuccess) {
     cfg.gridDim = dim3(unsigned(T * h->Hkv * h->kern.merge_slices));

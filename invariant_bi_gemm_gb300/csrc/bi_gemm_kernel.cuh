@@ -415,9 +415,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int kb = uc.kb_begin; kb < uc.kb_end && pre < C::STAGES; ++kb, ++pre)
               issue(pre, uc, kb, true, false);
           }
-  #ifdef BI_GEMM_TRIGGER_EARLY
-          ptx::launch_dependents();
-  #endif
         }
         ptx::grid_dependency_wait();
         int item = 0;

@@ -292,10 +292,12 @@ def test_tma_page_boxes_and_row_copies_give_the_same_bits():
 
 @pytest.mark.parametrize("lens", [[32768], [4096] * 8, [28672], [3000] * 20])
 def test_kernel_choice_changes_no_bit(lens):
-    """A call whose units fit in one round of the row-copy kernel's blocks but not of the TMA
-    kernel's runs the row-copy kernel (batch 1 x 32768 and 8 x 4096: 512 units); smaller and
-    larger calls run the TMA kernel.  Whichever the product picks, the bits are those of both
-    kernels pinned, and the request alone (batch 1) gives the same bits as inside its batch."""
+    """A call whose units fit in one round of the TMA kernel's four-block variant but not of its
+    three-block one runs the four-block variant (batch 1 x 32768 and 8 x 4096: 512 units);
+    smaller calls run the three-block variant in one round (batch 1 x 28672: 448 units), larger
+    ones persistently (20 x 3000).  Whichever the product picks, the bits are those of the TMA
+    and the row-copy kernels pinned, and the request alone (batch 1) gives the same bits as
+    inside its batch."""
     Hq, Hkv, D = 32, 8, 128
     bt = decode_batch(lens, Hq, Hkv, D, 16)
     attn = BiAttention(Hq, Hkv, D, 16)
