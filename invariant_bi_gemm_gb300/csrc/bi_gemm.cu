@@ -50,6 +50,8 @@ struct KernelInfo {
   const void* fn = nullptr;
   int threads = 0, smem = 0, tmem_cols = 0, stages = 0, bn = 0, bk = 0, mma_k = 0, ctas = 1;
   int w_box_cols = 0, w_swizzle = 128;   // TMA box width of W (columns) and its swizzle span
+  bool smallm = false;                   // has the small-M pipeline (bf16 pair tile)
+  int ring_bytes = 0, b_bytes = 0;       // its ring and one W tile (bytes per CTA)
 };
 
 template <class C>
@@ -66,6 +68,9 @@ KernelInfo info_of() {
   k.ctas = C::CTAS;
   k.w_box_cols = C::ATOM_N;
   k.w_swizzle = C::B_SW;
+  k.smallm = C::SMALLM;
+  k.ring_bytes = C::RING_BYTES;
+  k.b_bytes = C::B_BYTES;
   return k;
 }
 
@@ -300,6 +305,20 @@ int launch_core(bi_gemm* h, const void* x, int64_t M, const void* W, const bi_ge
   const int64_t x_bytes = M * h->K * (fp8 ? 1 : 2);
   p.group_n = int32_t(x_bytes <= kRasterXResidentBytes ? 1 : std::min<int64_t>(kRasterGroupN, h->n_tiles));
   p.w_early = (h->flags & BI_GEMM_FLAG_STATIC_W) ? 1 : 0;
+  // Small M on the pair tile (an x box of at most 64 rows): stages of two k-blocks laid out from
+  // the x box's rows, as many as the ring holds (at most STAGES - 1), keeping an MMA's 128-row x
+  // read of the last slot inside the ring.  A pipeline choice: no instruction, operand or order
+  // changes.
+  if (h->kern.smallm && a_box_rows <= 64) {
+    const int slot = int(a_box_rows) * 128 + h->kern.b_bytes;
+    int st = std::min(h->kern.stages - 1, h->kern.ring_bytes / (2 * slot));
+    while (st > 2 && (2 * st - 1) * slot + kBM * 128 > h->kern.ring_bytes) --st;
+    if (st >= 2 && (2 * st - 1) * slot + kBM * 128 <= h->kern.ring_bytes) {
+      p.small_m = 1;
+      p.small_stages = st;
+      p.slot_bytes = uint32_t(slot);
+    }
+  }
   p.timeout_ns = h->timeout_ns;
   p.test_flags = test_flags;
 

@@ -16,7 +16,9 @@
 //   * rows beyond M are zero-filled by TMA and never stored; a row's products never meet
 //     another row's, so neither M nor the other rows' contents can reach row i.
 // The persistent tile order (which SM computes which tile, and when) does change with M,
-// but it decides no arithmetic: a tile's value is the same wherever it runs.
+// but it decides no arithmetic: a tile's value is the same wherever it runs.  So does the
+// pipeline's grouping on the pair tile (two k-blocks a stage when the x box has at most 64
+// rows), which changes when the issuer waits, not which MMAs it issues or in what order.
 //
 // Tile = 128 x BN per CTA, or 256 x BN per CTA pair (CTAS = 2, BN = 256): the pair issues one
 // tcgen05.mma.cta_group::2 of M=256, each CTA staging its own 128 rows of x and its own BN/2
@@ -72,6 +74,9 @@ struct KParams {
                             // large: the S split CTAs of a sub-tile share it (else the last to
                             // arrive merges alone)
   int32_t w_early;          // W may be loaded before the previous kernel in the stream completes
+  int32_t small_m;          // bf16 pair tile, x box of at most 64 rows: the small-M pipeline below
+  int32_t small_stages;     // its stages (two k-blocks each)
+  uint32_t slot_bytes;      // its k-block slot: the x box's rows, then the W tile
   uint64_t timeout_ns;
   uint32_t test_flags;      // only read by the control build
 };
@@ -108,6 +113,12 @@ struct KCfg {
   static constexpr int A_BYTES = kBM * 128;             // 16 KB
   static constexpr int B_ATOM_BYTES = BK * B_SW;
   static constexpr int B_BYTES = N_ATOMS * B_ATOM_BYTES;
+  // Small-M pipeline (bf16 pair tile, x box of at most 64 rows): the same ring holds stages of
+  // two k-blocks, each k-block a slot of the x box's rows followed by its W tile, so that the MMA
+  // issuer waits once per eight MMAs and more bytes are in flight than six full stages allow.
+  // The instructions, their operands and their order are those of the other pipeline.
+  static constexpr bool SMALLM = !kFp8 && CTAS == 2;
+  static constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES);
   static constexpr int SFA_BYTES = kFp8 ? 512 : 0;      // 128 rows x 4 k-blocks
   // Each CTA stages the scales of all BN columns: on a pair, the block-scaled MMA reads the B
   // scales of the whole N extent from each CTA's own TMEM.
@@ -399,45 +410,119 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           issued_mask |= 1u << st;
           issued_par = (issued_par & ~(1u << st)) | (phase << st);
         };
-        // W is only read.  When the caller has declared that no kernel which may still be running
-        // writes it (p.w_early), the W tiles of this CTA's first STAGES k-blocks are issued before
-        // the wait for the previous kernel in the stream; only x (which may be that kernel's
-        // output) and every later load wait for it.  The stages are fresh, so no empty-barrier
-        // wait is needed for them.
-        int pre = 0;
-        bool early = p.w_early != 0;
-  #ifdef BI_GEMM_CONTROLS
-        early = early && !(p.test_flags & 1u);
-  #endif
-        if (early) {
-          for (int u = group; u < units && pre < C::STAGES; u += ngroups) {
-            const UnitCoord uc = unit_coord(u, p);
-            for (int kb = uc.kb_begin; kb < uc.kb_end && pre < C::STAGES; ++kb, ++pre)
-              issue(pre, uc, kb, true, false);
-          }
-        }
-        ptx::grid_dependency_wait();
-        int item = 0;
-        for (int u = group; u < units && ok; u += ngroups) {
-          const UnitCoord uc = unit_coord(u, p);
-          for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb, ++item) {
-            if (item < pre) {
-              issue(stage, uc, kb, false, true);          // its W is already on the way
-            } else {
-              if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
-                ok = false;
-                break;
+        bool small_done = false;
+        if constexpr (C::SMALLM) {
+         if (p.small_m) {
+          // Small-M pipeline: stage st holds k-blocks kb, kb + 1 in slots 2st, 2st + 1, each the
+          // x box's rows followed by the W tile; otherwise as below.
+          const int nst = p.small_stages;
+          const uint32_t a_bytes = uint32_t(p.a_box_rows) * 128u;
+          auto issue2 = [&](int st, const UnitCoord& uc, int kb, int nsub, bool w_part, bool x_part) {
+            const uint32_t fb = full_bar(st);
+            const uint32_t lfb = ptx::mapa_shared(fb, 0);   // the leader's full barrier
+            const int row0 = uc.m_tile * C::TILE_M + int(rank) * kBM;
+            const int col0 = uc.n_tile * C::BN + int(rank) * C::BN_CTA;
+            const bool load_a = row0 < p.M;              // (the peer's rows all lie past M here)
+            if (w_part && rank == 0)
+              ptx::mbar_arrive_expect_tx(fb, uint32_t(nsub) * ((load_a ? a_bytes : 0u) + uint32_t(C::CTAS * C::B_BYTES)));
+  #pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              if (j < nsub) {
+                const uint32_t adst = sbase + uint32_t(st * 2 + j) * p.slot_bytes;
+                const uint32_t bdst = adst + p.slot_bytes - uint32_t(C::B_BYTES);
+                const int kc = (kb + j) * C::BK;
+                if (x_part && load_a) ptx::tma_load_2d_pair(adst, &tmap_x, lfb, kc, row0);
+                if (w_part) {
+  #pragma unroll
+                  for (int a = 0; a < C::N_ATOMS; ++a)
+                    ptx::tma_load_2d_pair(bdst + a * C::B_ATOM_BYTES, &tmap_w, lfb, col0 + a * C::ATOM_N, kc);
+                }
               }
-              bool skip = false;
-  #ifdef BI_GEMM_CONTROLS
-              // control build only: withhold one stage so that the consumer's bounded wait expires
-              skip = (p.test_flags & 1u) && u == group && kb == uc.kb_begin;
-  #endif
-              if (!skip) issue(stage, uc, kb, true, true);
             }
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1u;
+            issued_mask |= 1u << st;
+            issued_par = (issued_par & ~(1u << st)) | (phase << st);
+          };
+          int pre = 0;
+          bool early = p.w_early != 0;
+  #ifdef BI_GEMM_CONTROLS
+          early = early && !(p.test_flags & 1u);
+  #endif
+          if (early) {
+            for (int u = group; u < units && pre < nst; u += ngroups) {
+              const UnitCoord uc = unit_coord(u, p);
+              for (int kb = uc.kb_begin; kb < uc.kb_end && pre < nst; kb += 2, ++pre)
+                issue2(pre, uc, kb, min(2, uc.kb_end - kb), true, false);
+            }
+          }
+          ptx::grid_dependency_wait();
+          int item = 0;
+          for (int u = group; u < units && ok; u += ngroups) {
+            const UnitCoord uc = unit_coord(u, p);
+            for (int kb = uc.kb_begin; kb < uc.kb_end; kb += 2, ++item) {
+              const int nsub = min(2, uc.kb_end - kb);
+              if (item < pre) {
+                issue2(stage, uc, kb, nsub, false, true);
+              } else {
+                if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
+                  ok = false;
+                  break;
+                }
+                bool skip = false;
+  #ifdef BI_GEMM_CONTROLS
+                skip = (p.test_flags & 1u) && u == group && kb == uc.kb_begin;
+  #endif
+                if (!skip) issue2(stage, uc, kb, nsub, true, true);
+              }
+              if (++stage == nst) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+          small_done = true;
+         }
+        }
+        if (!small_done) {
+          // W is only read.  When the caller has declared that no kernel which may still be running
+          // writes it (p.w_early), the W tiles of this CTA's first STAGES k-blocks are issued before
+          // the wait for the previous kernel in the stream; only x (which may be that kernel's
+          // output) and every later load wait for it.  The stages are fresh, so no empty-barrier
+          // wait is needed for them.
+          int pre = 0;
+          bool early = p.w_early != 0;
+    #ifdef BI_GEMM_CONTROLS
+          early = early && !(p.test_flags & 1u);
+    #endif
+          if (early) {
+            for (int u = group; u < units && pre < C::STAGES; u += ngroups) {
+              const UnitCoord uc = unit_coord(u, p);
+              for (int kb = uc.kb_begin; kb < uc.kb_end && pre < C::STAGES; ++kb, ++pre)
+                issue(pre, uc, kb, true, false);
+            }
+          }
+          ptx::grid_dependency_wait();
+          int item = 0;
+          for (int u = group; u < units && ok; u += ngroups) {
+            const UnitCoord uc = unit_coord(u, p);
+            for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb, ++item) {
+              if (item < pre) {
+                issue(stage, uc, kb, false, true);          // its W is already on the way
+              } else {
+                if (!wait_phase(empty_bar(stage), phase ^ 1u, sc, kErrTimeoutProducer)) {
+                  ok = false;
+                  break;
+                }
+                bool skip = false;
+    #ifdef BI_GEMM_CONTROLS
+                // control build only: withhold one stage so that the consumer's bounded wait expires
+                skip = (p.test_flags & 1u) && u == group && kb == uc.kb_begin;
+    #endif
+                if (!skip) issue(stage, uc, kb, true, true);
+              }
+              if (++stage == C::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+              }
             }
           }
         }
@@ -472,69 +557,124 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int buf = 0;
         uint32_t bphase = 0;
         bool ok = true, issued_any = false;
-        for (int u = group; u < units && ok; u += ngroups) {
-          const UnitCoord uc = unit_coord(u, p);
-          if (!wait_phase(tempty_bar(buf), bphase ^ 1u, sc, kErrTimeoutMma)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t d_tmem = tmem_base + uint32_t(buf * C::BN);
-          for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
-            if (!wait_phase(full_bar(stage), phase, sc, kErrTimeoutMma)) {
+        bool small_done = false;
+        if constexpr (C::SMALLM) {
+         if (p.small_m) {
+          // Small-M pipeline (see the producer): one wait and one commit per two k-blocks, the
+          // same MMAs in the same order as below.
+          const int nst = p.small_stages;
+          for (int u = group; u < units && ok; u += ngroups) {
+            const UnitCoord uc = unit_coord(u, p);
+            if (!wait_phase(tempty_bar(buf), bphase ^ 1u, sc, kErrTimeoutMma)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            const uint32_t a_addr = sbase + C::OFF_A + stage * C::A_BYTES;
-            const uint32_t b_addr = sbase + C::OFF_B + stage * C::B_BYTES;
-            if constexpr (C::kFp8) {
-              // the stage's scales are already in TMEM: their copies were committed to full_bar
-              const uint32_t sfa_t = tmem_base + uint32_t(C::SF_TMEM_COL0 + 16 * stage);
-              const uint32_t sfb_t = sfa_t + 8u;
-  #pragma unroll
-              for (int kk = 0; kk < C::K_STEPS; ++kk) {
-                const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
-                const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
-                                               8 * C::B_SW, C::B_LAYOUT);
-                const uint32_t idesc = C::IDESC_MXF8 | (uint32_t(kk) << 4) | (uint32_t(kk) << 29);
-                const uint32_t acc = (kb != uc.kb_begin || kk != 0) ? 1u : 0u;
-                if constexpr (kPair)
-                  ptx::mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
-                else
-                  ptx::mma_mxf8(d_tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
+            const uint32_t d_tmem = tmem_base + uint32_t(buf * C::BN);
+            for (int kb = uc.kb_begin; kb < uc.kb_end; kb += 2) {
+              if (!wait_phase(full_bar(stage), phase, sc, kErrTimeoutMma)) {
+                ok = false;
+                break;
               }
-            } else {
+              ptx::tc_fence_after();
+              const int nsub = min(2, uc.kb_end - kb);
   #pragma unroll
-              for (int kk = 0; kk < C::K_STEPS; ++kk) {
-                const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
-                const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
-                                               8 * C::B_SW, C::B_LAYOUT);
-                const uint32_t acc = (kb != uc.kb_begin || kk != 0) ? 1u : 0u;
-                if constexpr (kPair)
-                  ptx::mma_bf16_pair(d_tmem, ad, bd, C::IDESC_BF16, acc);
-                else
-                  ptx::mma_bf16(d_tmem, ad, bd, C::IDESC_BF16, acc);
+              for (int j = 0; j < 2; ++j) {
+                if (j < nsub) {
+                  const uint32_t a_addr = sbase + uint32_t(stage * 2 + j) * p.slot_bytes;
+                  const uint32_t b_addr = a_addr + p.slot_bytes - uint32_t(C::B_BYTES);
+  #pragma unroll
+                  for (int kk = 0; kk < C::K_STEPS; ++kk) {
+                    const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
+                    const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
+                                                   8 * C::B_SW, C::B_LAYOUT);
+                    const uint32_t acc = (kb + j != uc.kb_begin || kk != 0) ? 1u : 0u;
+                    ptx::mma_bf16_pair(d_tmem, ad, bd, C::IDESC_BF16, acc);
+                  }
+                }
+              }
+              issued_any = true;
+              ptx::tc_commit_pair_mc(empty_bar(stage), 0x3);   // frees the stage in both CTAs
+              if (++stage == nst) {
+                stage = 0;
+                phase ^= 1u;
               }
             }
-            issued_any = true;
-            if constexpr (kPair)
-              ptx::tc_commit_pair_mc(empty_bar(stage), 0x3);   // frees the stage in both CTAs
-            else
-              ptx::tc_commit(empty_bar(stage));
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1u;
+            if (!ok) break;
+            ptx::tc_commit_pair_mc(tfull_bar(buf), 0x3);       // both CTAs' epilogues
+            if (++buf == C::ACC_BUFS) {
+              buf = 0;
+              bphase ^= 1u;
             }
           }
-          if (!ok) break;
-          if constexpr (kPair)
-            ptx::tc_commit_pair_mc(tfull_bar(buf), 0x3);       // both CTAs' epilogues
-          else
-            ptx::tc_commit(tfull_bar(buf));
-          if (++buf == C::ACC_BUFS) {
-            buf = 0;
-            bphase ^= 1u;
+          small_done = true;
+         }
+        }
+        if (!small_done) {
+          for (int u = group; u < units && ok; u += ngroups) {
+            const UnitCoord uc = unit_coord(u, p);
+            if (!wait_phase(tempty_bar(buf), bphase ^ 1u, sc, kErrTimeoutMma)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t d_tmem = tmem_base + uint32_t(buf * C::BN);
+            for (int kb = uc.kb_begin; kb < uc.kb_end; ++kb) {
+              if (!wait_phase(full_bar(stage), phase, sc, kErrTimeoutMma)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              const uint32_t a_addr = sbase + C::OFF_A + stage * C::A_BYTES;
+              const uint32_t b_addr = sbase + C::OFF_B + stage * C::B_BYTES;
+              if constexpr (C::kFp8) {
+                // the stage's scales are already in TMEM: their copies were committed to full_bar
+                const uint32_t sfa_t = tmem_base + uint32_t(C::SF_TMEM_COL0 + 16 * stage);
+                const uint32_t sfb_t = sfa_t + 8u;
+    #pragma unroll
+                for (int kk = 0; kk < C::K_STEPS; ++kk) {
+                  const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
+                  const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
+                                                 8 * C::B_SW, C::B_LAYOUT);
+                  const uint32_t idesc = C::IDESC_MXF8 | (uint32_t(kk) << 4) | (uint32_t(kk) << 29);
+                  const uint32_t acc = (kb != uc.kb_begin || kk != 0) ? 1u : 0u;
+                  if constexpr (kPair)
+                    ptx::mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
+                  else
+                    ptx::mma_mxf8(d_tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
+                }
+              } else {
+    #pragma unroll
+                for (int kk = 0; kk < C::K_STEPS; ++kk) {
+                  const uint64_t ad = make_sdesc(a_addr + kk * 32, 16, 1024, kLayoutSW128);
+                  const uint64_t bd = make_sdesc(b_addr + kk * C::MMA_K * C::B_SW, C::B_ATOM_BYTES,
+                                                 8 * C::B_SW, C::B_LAYOUT);
+                  const uint32_t acc = (kb != uc.kb_begin || kk != 0) ? 1u : 0u;
+                  if constexpr (kPair)
+                    ptx::mma_bf16_pair(d_tmem, ad, bd, C::IDESC_BF16, acc);
+                  else
+                    ptx::mma_bf16(d_tmem, ad, bd, C::IDESC_BF16, acc);
+                }
+              }
+              issued_any = true;
+              if constexpr (kPair)
+                ptx::tc_commit_pair_mc(empty_bar(stage), 0x3);   // frees the stage in both CTAs
+              else
+                ptx::tc_commit(empty_bar(stage));
+              if (++stage == C::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+            if (!ok) break;
+            if constexpr (kPair)
+              ptx::tc_commit_pair_mc(tfull_bar(buf), 0x3);       // both CTAs' epilogues
+            else
+              ptx::tc_commit(tfull_bar(buf));
+            if (++buf == C::ACC_BUFS) {
+              buf = 0;
+              bphase ^= 1u;
+            }
           }
         }
         if (!ok && issued_any) {

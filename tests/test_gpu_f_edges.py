@@ -30,6 +30,13 @@ def test_empty_batch_is_noop():
     (8, 64, "bf16", 1),            # K = 8: one partial k-block
     (1024, 4000, "bf16", 300),     # N ends inside the second (peer) half of the last pair tile
     (1024, 4000, "bf16_f32", 77),
+    # pair tile at M <= 64 (stages of two k-blocks): an odd k-block count (the last stage holds
+    # one), a partial last k-block, a single k-block, a single stage, ragged N
+    (1032, 264, "bf16", 57),
+    (200, 200, "bf16", 13),
+    (8, 264, "bf16", 1),
+    (72, 264, "bf16_f32", 3),
+    (4096, 520, "bf16_f32", 64),
 ])
 def test_ragged_shapes(K, N, kind, M):
     x = ig.normal_bf16(21, M, K)
@@ -42,9 +49,10 @@ def test_ragged_shapes(K, N, kind, M):
     g.close()
 
 
-@pytest.mark.parametrize("kind,N,split", [("bf16", 200, 0), ("bf16_f32", 24, 0), ("bf16_f32", 40, 4)])
-def test_guard_bands(kind, N, split):
-    K, M = 1024, 77
+@pytest.mark.parametrize("kind,N,split,M", [("bf16", 200, 0, 77), ("bf16_f32", 24, 0, 77), ("bf16_f32", 40, 4, 77),
+                                            ("bf16", 520, 0, 33)])
+def test_guard_bands(kind, N, split, M):
+    K = 1024
     x = dev_bf16(ig.normal_bf16(31, M, K))
     w = dev_bf16(ig.normal_bf16(32, K, N, std=0.05))
     g = BiGemm(K, N, kind, split_k=split)

@@ -85,8 +85,9 @@ def test_n2_small_m_fork_control_fails(ctl):
     L.bi_ctl_destroy(h)
 
 
-def test_stalled_pipeline_reports_timeout_and_context_survives(ctl):
-    K, N, M = 1024, 256, 200
+@pytest.mark.parametrize("M", [200, 40])   # the pair tile's two pipelines (M = 40: two k-blocks a stage)
+def test_stalled_pipeline_reports_timeout_and_context_survives(ctl, M):
+    K, N = 1024, 256
     x = ig.normal_bf16(61, M, K)
     w = ig.normal_bf16(62, K, N, std=0.05)
     xd, wd = dev_bf16(x), dev_bf16(w)
