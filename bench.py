@@ -42,12 +42,12 @@ STATIC_W = True
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of each launch of the sweep, from one
 # ncu capture of `python bench.py --steps 1 --warmup 3 --no-paths --no-cpu` (the command and the
 # figures are in profiles/ncu_bf16_gemm_llm_sweep.md), for the kernel sources of the given hash.
-TRAFFIC = {"source_sha256_16": "7eb081cfb2d3ae24", "bytes_per_launch": {
-    1: 120480000, 7: 117983232, 8: 117764096, 15: 117652992,
-    16: 117676544, 17: 117715712, 63: 118142720, 64: 118158592,
-    65: 118145024, 128: 118604288, 129: 118596096, 192: 119118848,
-    193: 119199232, 256: 119720192, 512: 123275520, 1024: 141131520,
-    2048: 175838464, 4096: 280269824, 8192: 731410176}}
+TRAFFIC = {"source_sha256_16": "5e0865f4e411cb32", "bytes_per_launch": {
+    1: 120521216, 7: 117620992, 8: 117682688, 15: 117749248,
+    16: 117761792, 17: 117951744, 63: 118087168, 64: 118089728,
+    65: 118169856, 128: 118985984, 129: 118648064, 192: 119137536,
+    193: 119150592, 256: 119681536, 512: 123747072, 1024: 141447680,
+    2048: 174518016, 4096: 278937344, 8192: 739951616}}
 
 
 def flops(M, K=K_DIM, N=N_DIM):
