@@ -101,3 +101,28 @@ def test_split_too_large_for_merge_staging():
     assert np.array_equal(y1.view(np.uint32), y[3:4].view(np.uint32))
     assert g.device_error() == 0
     g.close()
+
+
+@pytest.mark.parametrize("kind", ["bf16", "bf16_f32"])
+def test_pair_tile_split_across_both_pipelines(kind):
+    """A wide single N tile with a long K (N = 256, K = 16384) runs the CTA-pair tile with the
+    fixed split of 32: rows of up to 64 take the pair tile's small-M pipeline (stages of two
+    k-blocks), larger batches the other one.  Every row of the M = 200 run against the oracle,
+    and every row bitwise the same at M = 1, 40, 64, 65 and 200, across the switch."""
+    K2, N2, M2 = 16384, 256, 200
+    x = ig.scaled_rows_bf16(71, M2, K2)
+    w = ig.normal_bf16(72, K2, N2, std=0.02)
+    g = BiGemm(K2, N2, kind)
+    c = g.config
+    assert c["ctas_per_tile"] == 2 and c["split_k"] == 32
+    out = "f32" if kind == "bf16_f32" else "bf16"
+    xd, wd = dev_bf16(x), dev_bf16(w)
+    y = host_bits(g(xd, wd))
+    y_ref, _, sabs = oracle.gemm_bf16(x, w, out)
+    check_tolerance(y, y_ref, sabs, oracle.TOL_F32 if out == "f32" else oracle.TOL_BF16, f"pair split {kind}")
+    view = np.uint32 if out == "f32" else np.uint16
+    for M in (1, 40, 64, 65):
+        yM = host_bits(g(xd[:M].contiguous(), wd))
+        assert np.array_equal(yM.view(view), y[:M].view(view)), (kind, M)
+    assert g.device_error() == 0
+    g.close()
