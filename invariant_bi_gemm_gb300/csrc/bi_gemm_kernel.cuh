@@ -128,6 +128,11 @@ struct KCfg {
   // MXFP8: six scale-producer warps take the k-blocks in turn, so that the load latency of six
   // stages' scales overlaps.
   static constexpr int SCALE_WARPS = kFp8 ? 6 : 0;
+  // Each scale warp owns one stage's scale slot (warp j fills items j, j + STAGES, ...), so a
+  // warp's wait for the slot's previous copy (a parity wait on sfdone_bar) can never see a phase
+  // two behind; with more scale warps than stages two warps would share a slot and that wait
+  // could pass on the wrong phase.
+  static_assert(!kFp8 || SCALE_WARPS == STAGES, "MXFP8: one scale warp per stage");
   static constexpr int NUM_WARPS = 2 + SCALE_WARPS + EPI_WARPS;
   static constexpr int EPI_WARP0 = NUM_WARPS - EPI_WARPS;
   // MXFP8 kernels launch 16 warps (128 registers a thread); setmaxnreg then moves registers from
