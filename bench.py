@@ -42,7 +42,7 @@ STATIC_W = True
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of each launch of the sweep, from one
 # ncu capture of `python bench.py --steps 1 --warmup 3 --no-paths --no-cpu` (the command and the
 # figures are in profiles/ncu_bf16_gemm_llm_sweep.md), for the kernel sources of the given hash.
-TRAFFIC = {"source_sha256_16": "5e0865f4e411cb32", "bytes_per_launch": {
+TRAFFIC = {"source_sha256_16": "2f8d761ab6d68369", "bytes_per_launch": {
     1: 120521216, 7: 117620992, 8: 117682688, 15: 117749248,
     16: 117761792, 17: 117951744, 63: 118087168, 64: 118089728,
     65: 118169856, 128: 118985984, 129: 118648064, 192: 119137536,
