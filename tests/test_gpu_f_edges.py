@@ -37,6 +37,11 @@ def test_empty_batch_is_noop():
     (8, 264, "bf16", 1),
     (72, 264, "bf16_f32", 3),
     (4096, 520, "bf16_f32", 64),
+    # more N tiles than CTA pairs (80 and 81 tiles on 76 pairs): some pairs run two tiles, in
+    # both pipelines, the second tile's accumulator double-buffered behind the first
+    (512, 20480, "bf16", 40),
+    (520, 20488, "bf16_f32", 64),
+    (512, 20480, "bf16", 200),
 ])
 def test_ragged_shapes(K, N, kind, M):
     x = ig.normal_bf16(21, M, K)
