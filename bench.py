@@ -775,10 +775,13 @@ def measure_attention(dev, peaks):
                      "position context-1, split size 512 positions",
             "grid_bound": cfg["max_ctas"], "rows": rows, "device_error": err,
             "kernel": ("TMA page boxes: a producer warp and four consumer warps per block, "
-                       f"{cfg['ring_stages']}-stage ring" if cfg["tma_pages"] else
+                       f"{cfg['ring_stages']}-stage ring at three blocks per SM; a call that fits one round of "
+                       "four blocks per SM but not of three (the 512-unit shapes here) runs the same kernel built "
+                       "for four, with a 2-stage ring" if cfg["tma_pages"] else
                        f"cp.async row copies, {cfg['ring_stages']}-stage ring") + f", {cfg['threads']} threads",
             "bytes": "K and V of every request once (2 x B x context x 8 x 128 x 2) + q and o",
-            "note": "graph-timed; pages shuffled over the cache; three kernels per call (plan, attention, merge)"}
+            "note": "graph-timed; pages shuffled over the cache; two kernels per call (attention, merge), plus a "
+                    "plan kernel for calls of more than 32 tokens"}
 
 
 RMS_D = 4096
