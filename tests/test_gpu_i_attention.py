@@ -171,9 +171,11 @@ def test_negative_control_batch_keyed_split_size_is_caught():
         a.close()
 
 
-def test_long_context_sampled():
+@pytest.mark.parametrize("lens", [[32768, 8192, 1], [32768], [4096] * 8])
+def test_long_context_sampled(lens):
+    """Long contexts against the oracle: a call of 648 units (the three-block TMA kernel over
+    more than one round) and two calls of 512 units (one round of the four-block build)."""
     Hq, Hkv, D = 32, 8, 128
-    lens = [32768, 8192, 1]
     bt = decode_batch(lens, Hq, Hkv, D, 16)
     attn = BiAttention(Hq, Hkv, D, 16)
     o = bt.run(attn)
