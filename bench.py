@@ -502,8 +502,10 @@ def measure_e2e(g, W_np, X_np, args, dev, world):
     x[:M] from pinned host memory, runs, and reads each y[:M] back to pinned host memory.  The
     copies are pipelined with the GEMMs as a user would: host-to-device copies on one stream,
     GEMMs on the compute stream, device-to-host copies on a third, ordered by events.  Each
-    launch has its own x and y regions and W alternates between two buffers from step to step,
-    so that no copy overwrites data a running GEMM still reads."""
+    launch has its own x and y regions, and W, x and y alternate between two device buffers from
+    step to step: a step's copies into a buffer wait for the GEMMs of the step that last read it,
+    and its GEMMs wait for the read-back of the step that last wrote its y, so that no copy or
+    GEMM touches data another one still uses."""
     import numpy as np
     import torch
     steps = max(2, min(args.steps, 10))
@@ -518,37 +520,42 @@ def measure_e2e(g, W_np, X_np, args, dev, world):
         Xh[off:off + M] = torch.from_numpy(X_np[:M].view(np.int16)).view(torch.bfloat16)
     Yh = torch.empty((rows, N_DIM), dtype=torch.bfloat16).pin_memory()
     Wd = [torch.empty_like(Wh, device=dev) for _ in range(2)]
-    Xd = torch.empty((rows, K_DIM), dtype=torch.bfloat16, device=dev)
-    Yd = torch.empty((rows, N_DIM), dtype=torch.bfloat16, device=dev)
+    Xd = [torch.empty((rows, K_DIM), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    Yd = [torch.empty((rows, N_DIM), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     comp = torch.cuda.current_stream(dev)
     h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    state = {"w_free": [None, None], "last": None}
+    # per buffer set: the GEMMs of the step that last read its W and x, the read-back of the step
+    # that last wrote its y
+    state = {"in_free": [None, None], "out_free": [None, None], "last": None}
 
     def step(s):
-        wb = s % 2
+        b = s % 2
         with torch.cuda.stream(h2d):
-            if state["w_free"][wb] is not None:
-                h2d.wait_event(state["w_free"][wb])       # the GEMMs of step s-2 read this W
-            Wd[wb].copy_(Wh, non_blocking=True)
+            if state["in_free"][b] is not None:
+                h2d.wait_event(state["in_free"][b])       # the GEMMs of step s-2 read this W and x
+            Wd[b].copy_(Wh, non_blocking=True)
             xs = []
             for M, off in zip(M_SWEEP, offs):
-                Xd[off:off + M].copy_(Xh[off:off + M], non_blocking=True)
+                Xd[b][off:off + M].copy_(Xh[off:off + M], non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(h2d)
                 xs.append(ev)
+        if state["out_free"][b] is not None:
+            comp.wait_event(state["out_free"][b])         # step s-2's y has been read back
         for i, (M, off) in enumerate(zip(M_SWEEP, offs)):
             comp.wait_event(xs[i])
-            g(Xd[off:off + M], Wd[wb], Yd[off:off + M], stream=comp)
+            g(Xd[b][off:off + M], Wd[b], Yd[b][off:off + M], stream=comp)
             done = torch.cuda.Event()
             done.record(comp)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(done)
-                Yh[off:off + M].copy_(Yd[off:off + M], non_blocking=True)
+                Yh[off:off + M].copy_(Yd[b][off:off + M], non_blocking=True)
         free = torch.cuda.Event()
         free.record(comp)
-        state["w_free"][wb] = free
+        state["in_free"][b] = free
         last = torch.cuda.Event()
         last.record(d2h)
+        state["out_free"][b] = last
         state["last"] = last
 
     step(0)
@@ -569,7 +576,7 @@ def measure_e2e(g, W_np, X_np, args, dev, world):
     # the pipelined results are the GEMM's: compare a few launches with a direct device run
     for i in (0, len(M_SWEEP) // 2, len(M_SWEEP) - 1):
         M, off = M_SWEEP[i], offs[i]
-        ref = g(Xd[off:off + M], Wd[0])
+        ref = g(Xd[0][off:off + M], Wd[0])
         assert torch.equal(Yh[off:off + M].view(torch.int16), ref.cpu().view(torch.int16)), f"e2e M={M}"
     h2d_bytes = 2 * K_DIM * N_DIM + sum(2 * M * K_DIM for M in M_SWEEP)
     d2h_bytes = sum(2 * M * N_DIM for M in M_SWEEP)
@@ -583,9 +590,9 @@ def measure_e2e(g, W_np, X_np, args, dev, world):
     for s in range(steps):
         with torch.cuda.stream(h2d):
             Wd[s % 2].copy_(Wh, non_blocking=True)
-            Xd.copy_(Xh, non_blocking=True)
+            Xd[s % 2].copy_(Xh, non_blocking=True)
         with torch.cuda.stream(d2h):
-            Yh.copy_(Yd, non_blocking=True)
+            Yh.copy_(Yd[s % 2], non_blocking=True)
     comp.wait_stream(h2d)
     comp.wait_stream(d2h)
     c1.record(comp)
@@ -596,8 +603,10 @@ def measure_e2e(g, W_np, X_np, args, dev, world):
             "copies_only_ms_per_step": round(link_ms, 3),
             "copies_only_gbs": round((h2d_bytes + d2h_bytes) / (link_ms / 1e3) / 1e9, 1),
             "how": "pinned host buffers; host-to-device copies, GEMMs and device-to-host copies on three "
-                   "streams ordered by events (copies overlap GEMMs of other launches); copies_only: the "
-                   "same bytes copied both ways at once without the GEMMs, the host link's own time"}
+                   "streams ordered by events (copies overlap GEMMs of other launches; W, x and y in two "
+                   "device buffer sets used by alternate steps, each reuse ordered after the last use); "
+                   "copies_only: the same bytes copied both ways at once without the GEMMs, the host "
+                   "link's own time"}
 
 
 def measure_other_paths(dev, peaks):
