@@ -189,13 +189,13 @@ struct Cfg {
   static constexpr int ROW_BYTES = D * 2;
   static constexpr int STAGE_BYTES = kStagePos * ROW_BYTES;
   static constexpr int CHUNKS_PER_THREAD = kStagePos * CHUNKS / kThreads;
-  static constexpr int NT1 = kStagePos / 4 / 8;        // score n tiles (8 positions) per warp
+  static constexpr int WPOS = kStagePos / 4;           // positions of a stage per warp (one m tile)
   static constexpr int QS = D + 8;                     // query row stride in shared memory
   static constexpr int KSTEPS = D / 16;                // k steps of the score MMA
   static constexpr int DW = D / 4;                     // output dimensions per warp
-  static constexpr int NT2 = DW / 8;                   // n tiles per warp in the value MMA
-  static_assert(G <= 8, "the query heads of a group fill at most 8 of the MMA's 16 rows");
-  static_assert(NT2 % 2 == 0, "n tiles are loaded in pairs");
+  static constexpr int MT2 = DW / 16;                  // m tiles (16 dimensions) per warp in the value MMA
+  static_assert(G <= 8, "the query heads of a group fill at most the MMA's 8 columns");
+  static_assert(WPOS == 16 && MT2 >= 1 && DW % 16 == 0, "warp layout: 16 positions, 16-dimension tiles");
   // score row stride (floats): a multiple of 8 keeps float2 rows aligned; +8 spreads the banks
   __host__ __device__ static int sc_stride(int split) { return split + 8; }
   // ring | row offsets [2][split] (int64) | scores [G][stride] | per-warp maxima [G][4] |
@@ -225,13 +225,20 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
 }
 
 // d += a * b on the tensor cores: a 16 x 16 (row-major, bf16), b 16 x 8 (column-major, bf16),
-// d 16 x 8 fp32.  Rows 8..15 of a are zero here (a1 = a3 = 0): the query heads use rows 0..7.
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+// d 16 x 8 fp32.  Both passes put the G <= 8 query heads of a unit on the 8 columns (n) and 16
+// positions (scores) or 16 output dimensions (values) on the rows (m), so that every row of the
+// instruction carries data:
+//   scores  S^T = K Q^T:  a = 16 key rows x 16 dimensions, b = the query rows (column = head);
+//   values  O^T += V^T P^T:  a = 16 dimensions x 16 value rows, b = the weights (column = head).
+// Fragment coordinates (gq = lane / 4, tq = lane % 4): a0 = a[gq][2tq, +1], a1 = a[gq + 8][2tq, +1],
+// a2 = a[gq][2tq + 8, +1], a3 = a[gq + 8][2tq + 8, +1]; b0 = b[2tq, +1][gq], b1 = b[2tq + 8, +1][gq];
+// d0, d1 = d[gq][2tq, +1], d2, d3 = d[gq + 8][2tq, +1].
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // One unit's coordinates, read from the plan.
@@ -314,6 +321,40 @@ __device__ __forceinline__ int4 plan_find(const Params& p, const PlanRegs& r, in
   }
   *total = carry;
   return rec;
+}
+
+// A unit's outputs from the value accumulators of one warp (acc[mt][e]: head 2tq + (e & 1),
+// dimension dbase + 16mt + gq + 8(e >> 1)): o = bf16(acc / l) for a single-split token, or the
+// fp32 partial sums of the split.
+template <int D, int G, int MT2>
+__device__ __forceinline__ void store_out(const Params& p, const Unit& w, const float (&acc)[MT2][4],
+                                          const float* hl, int dbase, int lane) {
+  const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int h = 2 * tq + (e & 1);
+    if (h < G) {
+      const float l = hl[h];
+      uint16_t* orow = p.o + (w.t * p.Hq + int64_t(w.kh) * G + h) * D + dbase + gq + (e >> 1) * 8;
+#pragma unroll
+      for (int mt = 0; mt < MT2; ++mt) orow[16 * mt] = uint16_t(pack_bf16x2(__fdiv_rn(acc[mt][e], l), 0.0f));
+    }
+  }
+}
+
+template <int D, int G, int MT2>
+__device__ __forceinline__ void store_partial(const Params& p, int64_t slot, const float (&acc)[MT2][4], int dbase,
+                                              int lane) {
+  const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int h = 2 * tq + (e & 1);
+    if (h < G) {
+      float* prow = p.part + (slot * G + h) * D + dbase + gq + (e >> 1) * 8;
+#pragma unroll
+      for (int mt = 0; mt < MT2; ++mt) prow[16 * mt] = acc[mt][e];
+    }
+  }
 }
 
 template <int D, int G, bool kInline>
@@ -445,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
       fetch_next();
       __syncthreads();   // the next unit's row offsets are visible to every issuing thread
     }
-    float acc[C::NT2][4];
+    float acc[C::MT2][4];
 #pragma unroll
-    for (int n = 0; n < C::NT2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+    for (int n = 0; n < C::MT2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
     for (int i = 0; i < nload; ++i) {
       const int ahead = i + kStages - 1;   // the load issued now: this unit's, or the next's
       if (ahead < nload) issue(cur, half, ahead, int(seq % kStages));
@@ -460,30 +501,24 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
       const uint32_t stage = ptx::smem_u32(ring + (cons % kStages) * C::STAGE_BYTES);
       ++cons;
       if (i < cur.nsub) {
-        // pass 1: scores of this warp's quarter of the stage, S = Q K^T on the tensor cores,
-        // fixed k order; row gq (a query head) of each n tile, columns 2tq and 2tq + 1
-        const int pos0 = i * kStagePos + warp * (kStagePos / 4);
-        // query A fragments: a0 = q[gq][16k + 2tq, +1], a2 = q[gq][16k + 8 + 2tq, +1]
+        // pass 1: scores of this warp's 16 positions of the stage, S^T = K Q^T on the tensor
+        // cores, fixed k order: rows gq and gq + 8 (positions), columns 2tq and 2tq + 1 (heads)
+        const int pos0 = i * kStagePos + warp * C::WPOS;
+        // query B fragments: b0 = q[gq][16k + 2tq, +1], b1 = q[gq][16k + 8 + 2tq, +1] (zero past the G heads)
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qsm + (half * G + (row_ok ? gq : 0)) * C::QS);
+        // key A fragments: the four 8 x 8 blocks (rows 0-7 | 8-15) x (dimensions 0-7 | 8-15) of the k step
+        const int prow = warp * C::WPOS + ((lane >> 3) & 1) * 8 + (lane & 7);
+        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int nt = 0; nt < C::NT1; ++nt) {
-          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          const int prow = warp * (kStagePos / 4) + nt * 8 + (lane & 7);
+        for (int k = 0; k < C::KSTEPS; ++k) {
+          uint32_t a[4];
+          ldsm_x4(chunk_addr(stage, prow, 2 * k + (lane >> 4)), a);
+          mma16816(d, a, row_ok ? qrow[8 * k + tq] : 0u, row_ok ? qrow[8 * k + 4 + tq] : 0u);
+        }
 #pragma unroll
-          for (int kp = 0; kp < C::KSTEPS / 2; ++kp) {
-            uint32_t b[4];
-            ldsm_x4(chunk_addr(stage, prow, 4 * kp + (lane >> 3)), b);
-            const int k0 = 2 * kp, k1 = 2 * kp + 1;
-            const uint32_t a00 = row_ok ? qrow[8 * k0 + tq] : 0u, a02 = row_ok ? qrow[8 * k0 + 4 + tq] : 0u;
-            const uint32_t a10 = row_ok ? qrow[8 * k1 + tq] : 0u, a12 = row_ok ? qrow[8 * k1 + 4 + tq] : 0u;
-            mma16816(d, a00, a02, b[0], b[1]);
-            mma16816(d, a10, a12, b[2], b[3]);
-          }
-          const int jl = pos0 + nt * 8 + 2 * tq;
-          if (row_ok) {
-            if (jl < cur.valid) sc[gq * SCS + jl] = __fmul_rn(d[0], p.c);
-            if (jl + 1 < cur.valid) sc[gq * SCS + jl + 1] = __fmul_rn(d[1], p.c);
-          }
+        for (int e = 0; e < 4; ++e) {
+          const int h = 2 * tq + (e & 1), jl = pos0 + gq + (e >> 1) * 8;
+          if (h < G && jl < cur.valid) sc[h * SCS + jl] = __fmul_rn(d[e], p.c);
         }
         if (i == cur.nsub - 1) {
           // the split's maximum per head, the weights in place and their sum (fixed tree)
@@ -517,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
                                 redl[tid * 4 + 3]);
         }
       } else {
-        // pass 2: O += P V over this stage's positions, 16 at a time, on the tensor cores;
+        // pass 2: O^T += V^T P^T over this stage's positions, 16 at a time, on the tensor cores;
         // P (fp32) enters as two bf16 parts, hi = bf16(P) and lo = bf16(P - hi), each an MMA
         const int sub = i - cur.nsub;
         const int rows = min(kStagePos, cur.valid - sub * kStagePos);
@@ -537,40 +572,29 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
             const float h0 = __uint_as_float(ah[h2] << 16), h1 = __uint_as_float(ah[h2] & 0xFFFF0000u);
             al[h2] = pack_bf16x2(__fsub_rn(x0, h0), __fsub_rn(x1, h1));
           }
+          // value A fragments (transposed loads): the blocks (positions 0-7 | 8-15) x
+          // (dimensions 0-7 | 8-15) of the m tile; the weights are the B fragments
 #pragma unroll
-          for (int np = 0; np < C::NT2 / 2; ++np) {
-            uint32_t b[4];
-            const int prow = k0 + ((lane >> 3) & 1) * 8 + (lane & 7);
-            ldsm_x4_trans(chunk_addr(stage, prow, (dbase + 16 * np) / 8 + (lane >> 4)), b);
-            mma16816(acc[2 * np], ah[0], ah[1], b[0], b[1]);
-            mma16816(acc[2 * np], al[0], al[1], b[0], b[1]);
-            mma16816(acc[2 * np + 1], ah[0], ah[1], b[2], b[3]);
-            mma16816(acc[2 * np + 1], al[0], al[1], b[2], b[3]);
+          for (int mt = 0; mt < C::MT2; ++mt) {
+            uint32_t a[4];
+            const int prow = k0 + (lane >> 4) * 8 + (lane & 7);
+            ldsm_x4_trans(chunk_addr(stage, prow, (dbase + 16 * mt) / 8 + ((lane >> 3) & 1)), a);
+            mma16816(acc[mt], a, ah[0], ah[1]);
+            mma16816(acc[mt], a, al[0], al[1]);
           }
         }
       }
       __syncthreads();
     }
 
-    // this thread's outputs: head gq, dimensions dbase + 8n + 2tq and + 1 for each n tile
-    const int64_t orow = (cur.t * p.Hq + int64_t(cur.kh) * G + gq) * D;
+    // this thread's outputs: heads 2tq and 2tq + 1, dimensions dbase + 16mt + gq and + 8 of
+    // each m tile
     if (cur.nsplit == 1) {
-      if (row_ok) {
-        const float l = hl[gq];
-#pragma unroll
-        for (int n = 0; n < C::NT2; ++n)
-          *reinterpret_cast<uint32_t*>(p.o + orow + dbase + 8 * n + 2 * tq) =
-              pack_bf16x2(__fdiv_rn(acc[n][0], l), __fdiv_rn(acc[n][1], l));
-      }
+      store_out<D, G>(p, cur, acc, hl, dbase, lane);
     } else {
       const int64_t slot0 = (cur.t * p.Hkv + cur.kh) * int64_t(p.max_splits);
       const int64_t slot = slot0 + cur.s;
-      if (row_ok) {
-#pragma unroll
-        for (int n = 0; n < C::NT2; ++n)
-          *reinterpret_cast<float2*>(p.part + (slot * G + gq) * D + dbase + 8 * n + 2 * tq) =
-              make_float2(acc[n][0], acc[n][1]);
-      }
+      store_partial<D, G>(p, slot, acc, dbase, lane);
       if (tid < G) {
         p.ml[(slot * G + tid) * 2 + 0] = hm[tid];
         p.ml[(slot * G + tid) * 2 + 1] = hl[tid];
@@ -597,16 +621,12 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const Params p) {
 // the consumers its query rows), so that no dependent load stalls the stream at a unit change.
 // Every wait on the ring is bounded: past the limit the block sets kErrTimeout, stops issuing,
 // waits (bounded) for the copies it has in flight, and leaves.
-// Consumer warps per block: CW = 4 (attn_kernel's layout) or 8 (head dimension 128 only).  With
-// 8 the positions of a stage and the dimensions of the output are spread over twice the warps;
-// every score and every output element still goes through the same instructions in the same
-// order, and the softmax reductions run on the first 128 consumer threads exactly as in
-// attn_kernel, so the bits do not change.  Four warps at three blocks per SM stream faster than
-// eight at two, so 4 is the choice.
-template <int D>
-constexpr int tma_consumer_warps() { return 4; }
-constexpr int tma_threads(int cw) { return 32 + 32 * cw; }
-constexpr int tma_blocks_per_sm(int cw) { return cw == 8 ? 2 : 3; }   // the ring is sized for these
+// Four consumer warps per block, each with the share of a stage (16 positions) and of the output
+// (D / 4 dimensions) that the same warp of attn_kernel has, so that every score and every output
+// element goes through the same instructions in the same order.  (Eight consumer warps at two
+// blocks per SM were measured slower than four at three.)
+constexpr int kTmaConsumerWarps = 4;
+constexpr int kTmaBlocksPerSm = 3;   // the ring of the default build is sized for these
 constexpr int kTmaMaxStages = 8;
 constexpr uint32_t kErrTimeout = 8u;          // a bounded wait on the ring expired
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -614,14 +634,11 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 template <int D, int G>
 struct TmaCfg {
   using C = Cfg<D, G>;
-  static constexpr int CW = tma_consumer_warps<D>();
+  static constexpr int CW = kTmaConsumerWarps;
   static constexpr int CT = 32 * CW;                   // consumer threads
-  static constexpr int THREADS = tma_threads(CW);
-  static constexpr int BLOCKS_PER_SM = tma_blocks_per_sm(CW);
-  static constexpr int NT1 = kStagePos / CW / 8;       // score n tiles (8 positions) per warp
-  static constexpr int DW = D / CW;                    // output dimensions per warp
-  static constexpr int NT2 = DW / 8;                   // n tiles per warp in the value MMA
-  static_assert(NT1 >= 1 && NT2 % 2 == 0 && CW >= 4, "consumer warp layout");
+  static constexpr int THREADS = 32 + CT;              // producer warp + consumers
+  static constexpr int BLOCKS_PER_SM = kTmaBlocksPerSm;
+  static_assert(CW == 4 && C::WPOS * CW == kStagePos, "consumer warp layout: attn_kernel's");
   static constexpr int HALVES = D / 64;                // 128-byte column halves of a row
   static constexpr int HALF_BYTES = kStagePos * 128;   // one half of a stage: 64 rows of 128 B
   static constexpr int STAGE_BYTES = HALVES * HALF_BYTES;
@@ -799,7 +816,7 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, kBlocksPerSm)
   const int ctid = tid - 32, cw = warp - 1;
   const int gq = lane >> 2, tq = lane & 3;
   const bool row_ok = gq < G;
-  const int dbase = cw * TC::DW;
+  const int dbase = cw * C::DW;
   constexpr int CT = TC::CT;
   // 16-byte chunk c of staged row r (the boxes' 128-byte swizzle: two column halves of 64 rows)
   auto chunk_addr = [&](uint32_t stage, int r, int c) {
@@ -845,9 +862,9 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, kBlocksPerSm)
     int4 nrec = make_int4(0, 0, 0, 0);
     Unit nxt = cur;
     const int nload = 2 * cur.nsub;
-    float acc[TC::NT2][4];
+    float acc[C::MT2][4];
 #pragma unroll
-    for (int n = 0; n < TC::NT2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+    for (int n = 0; n < C::MT2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
     for (int i = 0; i < nload; ++i, ++seq) {
       if (i == 0 && has_next) {
         if constexpr (kInline) plan_load(p, npr);
@@ -867,23 +884,20 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, kBlocksPerSm)
       const uint32_t stage = sbase + uint32_t(slot * TC::STAGE_BYTES);
       if (i < cur.nsub) {
         if (ok) {
-          const int pos0 = i * kStagePos + cw * (kStagePos / TC::CW);
+          // S^T = K Q^T for this warp's 16 positions, as in attn_kernel
+          const int pos0 = i * kStagePos + cw * C::WPOS;
+          const int prow = cw * C::WPOS + ((lane >> 3) & 1) * 8 + (lane & 7);
+          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-          for (int nt = 0; nt < TC::NT1; ++nt) {
-            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const int prow = cw * (kStagePos / TC::CW) + nt * 8 + (lane & 7);
+          for (int k = 0; k < C::KSTEPS; ++k) {
+            uint32_t a[4];
+            ldsm_x4(chunk_addr(stage, prow, 2 * k + (lane >> 4)), a);
+            mma16816(d, a, qa[k][0], qa[k][1]);
+          }
 #pragma unroll
-            for (int kp = 0; kp < C::KSTEPS / 2; ++kp) {
-              uint32_t b[4];
-              ldsm_x4(chunk_addr(stage, prow, 4 * kp + (lane >> 3)), b);
-              mma16816(d, qa[2 * kp][0], qa[2 * kp][1], b[0], b[1]);
-              mma16816(d, qa[2 * kp + 1][0], qa[2 * kp + 1][1], b[2], b[3]);
-            }
-            const int jl = pos0 + nt * 8 + 2 * tq;
-            if (row_ok) {
-              if (jl < cur.valid) sc[gq * SCS + jl] = __fmul_rn(d[0], p.c);
-              if (jl + 1 < cur.valid) sc[gq * SCS + jl + 1] = __fmul_rn(d[1], p.c);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const int h = 2 * tq + (e & 1), jl = pos0 + gq + (e >> 1) * 8;
+            if (h < G && jl < cur.valid) sc[h * SCS + jl] = __fmul_rn(d[e], p.c);
           }
         }
         if (i == cur.nsub - 1) {
@@ -957,14 +971,12 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, kBlocksPerSm)
               al[h2] = pack_bf16x2(__fsub_rn(x0, h0), __fsub_rn(x1, h1));
             }
 #pragma unroll
-            for (int np = 0; np < TC::NT2 / 2; ++np) {
-              uint32_t b[4];
-              const int prow = k0 + ((lane >> 3) & 1) * 8 + (lane & 7);
-              ldsm_x4_trans(chunk_addr(stage, prow, (dbase + 16 * np) / 8 + (lane >> 4)), b);
-              mma16816(acc[2 * np], ah[0], ah[1], b[0], b[1]);
-              mma16816(acc[2 * np], al[0], al[1], b[0], b[1]);
-              mma16816(acc[2 * np + 1], ah[0], ah[1], b[2], b[3]);
-              mma16816(acc[2 * np + 1], al[0], al[1], b[2], b[3]);
+            for (int mt = 0; mt < C::MT2; ++mt) {
+              uint32_t a[4];
+              const int prow = k0 + (lane >> 4) * 8 + (lane & 7);
+              ldsm_x4_trans(chunk_addr(stage, prow, (dbase + 16 * mt) / 8 + ((lane >> 3) & 1)), a);
+              mma16816(acc[mt], a, ah[0], ah[1]);
+              mma16816(acc[mt], a, al[0], al[1]);
             }
           }
         }
@@ -975,23 +987,11 @@ __global__ void __launch_bounds__(TmaCfg<D, G>::THREADS, kBlocksPerSm)
 
     named_bar_sync1<CT>();   // hl is written
     if (ok) {
-      const int64_t orow = (cur.t * p.Hq + int64_t(cur.kh) * G + gq) * D;
       if (cur.nsplit == 1) {
-        if (row_ok) {
-          const float l = hl[gq];
-#pragma unroll
-          for (int n = 0; n < TC::NT2; ++n)
-            *reinterpret_cast<uint32_t*>(p.o + orow + dbase + 8 * n + 2 * tq) =
-                pack_bf16x2(__fdiv_rn(acc[n][0], l), __fdiv_rn(acc[n][1], l));
-        }
+        store_out<D, G>(p, cur, acc, hl, dbase, lane);
       } else {
         const int64_t slot = (cur.t * p.Hkv + cur.kh) * int64_t(p.max_splits) + cur.s;
-        if (row_ok) {
-#pragma unroll
-          for (int n = 0; n < TC::NT2; ++n)
-            *reinterpret_cast<float2*>(p.part + (slot * G + gq) * D + dbase + 8 * n + 2 * tq) =
-                make_float2(acc[n][0], acc[n][1]);
-        }
+        store_partial<D, G>(p, slot, acc, dbase, lane);
         if (ctid < G) {
           p.ml[(slot * G + ctid) * 2 + 0] = hm[ctid];
           p.ml[(slot * G + ctid) * 2 + 1] = hl[ctid];
