@@ -1023,16 +1023,19 @@ template <int D, int G, int kMergeBatch>
 __global__ void __launch_bounds__(kMergeThreads, kMergeBatch <= 4 ? 4 : 2) merge_kernel(const Params p) {
   constexpr int kPairs = G * D / 2;
   constexpr int kSlices = (kPairs + kMergePairs - 1) / kMergePairs;
-  ptx::grid_dependency_wait();   // every unit's partial results are complete and visible
   const int64_t job = blockIdx.x / kSlices;             // token * Hkv + KV head
   const int slice = int(blockIdx.x - job * kSlices);
   const int64_t t = job / p.Hkv;
   const int32_t kh = int32_t(job - t * p.Hkv);
   if (t >= p.T) return;
-  const int32_t b = p.q_seq[t], pos = p.q_pos[t];
+  // The token's request and position are read before the wait for the attention kernel: that
+  // kernel does not write them, and this grid starts only after each of its blocks has passed its
+  // own wait for the kernels before it, so they are complete and visible (read from L2).
+  const int32_t b = __ldcg(p.q_seq + t), pos = __ldcg(p.q_pos + t);
   if (b < 0 || b >= p.B || pos < 0 || int64_t(pos / p.page_size) >= p.max_pages) return;
   const int32_t n = splits_of(pos, p.split);
   if (n == 1 || pos > p.max_pos) return;    // written directly / refused by the plan
+  ptx::grid_dependency_wait();   // every unit's partial results are complete and visible
   const int64_t slot0 = job * int64_t(p.max_splits);
   const int32_t c = (n + 3) / 4;
   const int pr = slice * kMergePairs + int(threadIdx.x >> 2), q = int(threadIdx.x & 3);
