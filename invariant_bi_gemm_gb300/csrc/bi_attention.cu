@@ -4,18 +4,19 @@
 // "Batch-invariant attention" (nondeterminism article): split the keys of a query at a fixed
 // split SIZE, reduce each split in one fixed order, merge the splits in a fixed order.  The
 // work unit is (query token t, KV head kh, split s); one block of 128 threads runs a unit:
-//   1. the G query heads of kh are held in registers as MMA A fragments;
+//   1. the G query heads of kh are held in registers as MMA B fragments (one column per head);
 //   2. the split's keys, then its values, stream through a 2-deep ring of 64-position stages
 //      (cp.async, 16-byte chunks, row-XOR swizzle so that the ldmatrix reads of both passes are
 //      free of bank conflicts); rows past p, or of an invalid page, are zero-filled and masked;
-//   3. pass 1: the G x 128 scores of a key stage, Q K^T on the tensor cores (mma.sync m16n8k16,
-//      bf16 in, fp32 accumulate; the G heads are rows 0..G-1 of the 16-row instruction, each
-//      warp 32 positions, k in ascending order), times scale * log2(e);
+//   3. pass 1: the 64 x G scores of a key stage, S^T = K Q^T on the tensor cores (mma.sync
+//      m16n8k16, bf16 in, fp32 accumulate; 16 key positions on the instruction's rows, the G <= 8
+//      heads on its columns, each warp 16 positions, k in ascending order), times scale * log2(e);
 //   4. per head, the split's maximum m (exact, order-free), the weights w_j = exp2(s_j - m) and
 //      their sum l (each thread its positions in order, then a fixed butterfly and warp order);
-//   5. pass 2: O += P V on the tensor cores, 16 positions per step in ascending order, each warp
-//      a quarter of the dimensions; the fp32 weights enter as two bf16 parts (hi = bf16(w),
-//      lo = bf16(w - hi), two MMAs), so the products carry 16 of the weights' bits, not 8;
+//   5. pass 2: O^T += V^T P^T on the tensor cores (16 output dimensions on the rows, the heads on
+//      the columns), 16 positions per step in ascending order, each warp a quarter of the
+//      dimensions; the fp32 weights enter as two bf16 parts (hi = bf16(w), lo = bf16(w - hi), two
+//      MMAs), so the products carry 16 of the weights' bits, not 8;
 //   6. a single-split token writes bf16(acc / l); otherwise the unit stores (m, l, acc), and a
 //      merge kernel combines the n splits of each (token, KV head): M = max m_s, then
 //      L = sum l_s 2^(m_s - M) and A = sum acc_s 2^(m_s - M) over four consecutive groups of
