@@ -68,6 +68,7 @@ def within(o_bits, v, a, e, D, L):
     (16, 2, 64, 16, 256),
     (8, 1, 128, 5, 512),
     (4, 4, 128, 16, 128),
+    (16, 8, 128, 8, 512),
 ])
 def test_parity_every_element(Hq, Hkv, D, page, split):
     lens = [1, 2, 127, 128, 129, 255, 256, 257, 700, 1500]
