@@ -11,10 +11,14 @@
 //   3. the T/32 warp partials are added in warp order, ((w0 + w1) + w2) + ...;
 //   4. mean = sum / d (correctly rounded division), r = correctly rounded 1/sqrt(mean + eps);
 //   5. y = bf16_rn((x * r) * g).
-// The kernel is HBM-bound (each row read once, written once): 16-byte streaming loads, the
-// next row of the block loaded while the current one is reduced, coalesced 16-byte stores,
-// a persistent grid of (resident blocks per SM) x (SMs) blocks striding over the rows, and a
-// programmatic dependent launch so that back-to-back kernels overlap their launch latency.
+// The kernel is HBM-bound (each row read once, written once): 16-byte streaming loads,
+// coalesced 16-byte stores and a programmatic dependent launch so that back-to-back kernels
+// overlap their launch latency.  Two builds of the same arithmetic: a persistent grid of
+// resident blocks striding over the rows, which loads a block's next row while it reduces the
+// current one, and a build without that prefetch capped at half the registers, so that twice as
+// many blocks fit on an SM; when the rows outnumber the first build's resident blocks but not the
+// second's, the second runs and every row has a block of its own.  Which build runs depends on
+// M; no operation on a row does.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -77,15 +81,16 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t xw, uint32_t gw, float r
   return pack_bf16x2(scaled(bf16_lo(xw), bf16_lo(gw), r), scaled(bf16_hi(xw), bf16_hi(gw), r));
 }
 
-// kOutF32 (test builds only): store the fp32 values before the bf16 rounding.
-template <bool kOutF32>
-__global__ void __launch_bounds__(kMaxThreads) rmsnorm_kernel(const Params p) {
+// kOutF32 (test builds only): store the fp32 values before the bf16 rounding.  kPrefetch: the
+// persistent build (a block's next row is loaded while the current one is reduced).
+template <bool kOutF32, bool kPrefetch = true>
+__global__ void __launch_bounds__(kMaxThreads, kPrefetch ? 1 : 2) rmsnorm_kernel(const Params p) {
   __shared__ float partial[2][kMaxThreads / 32];
   const int T = int(blockDim.x);
   const int t = int(threadIdx.x);
   const int lane = t & 31, warp = t >> 5, nwarps = T >> 5;
 
-  uint4 cur[kVecsPerThread], nxt[kVecsPerThread];
+  uint4 cur[kVecsPerThread], nxt[kPrefetch ? kVecsPerThread : 1];
   auto load_row = [&](int64_t row, uint4 (&dst)[kVecsPerThread]) {
     const uint4* src = p.x + row * p.nvec;
 #pragma unroll
@@ -106,7 +111,9 @@ __global__ void __launch_bounds__(kMaxThreads) rmsnorm_kernel(const Params p) {
   int buf = 0;
   for (; row < p.M; row += gridDim.x) {
     const int64_t next = row + gridDim.x;
-    if (next < p.M) load_row(next, nxt);   // in flight while this row is reduced
+    if constexpr (kPrefetch) {
+      if (next < p.M) load_row(next, nxt);   // in flight while this row is reduced
+    }
 
     // 1. this thread's squares, vectors and elements in ascending order
     float s = 0.0f;
@@ -151,8 +158,12 @@ __global__ void __launch_bounds__(kMaxThreads) rmsnorm_kernel(const Params p) {
         }
       }
     }
+    if constexpr (kPrefetch) {
 #pragma unroll
-    for (int j = 0; j < kVecsPerThread; ++j) cur[j] = nxt[j];
+      for (int j = 0; j < kVecsPerThread; ++j) cur[j] = nxt[j];
+    } else if (next < p.M) {
+      load_row(next, cur);
+    }
     buf ^= 1;
   }
 }
@@ -176,7 +187,8 @@ struct bi_rmsnorm {
   int device = 0;
   int threads = 0;
   int vecs_per_thread = 0;
-  int max_ctas = 0;
+  int max_ctas = 0;          // resident blocks of the persistent build
+  int max_ctas_single = 0;   // resident blocks of the one-row-per-block build
   int num_sms = 0;
 };
 
@@ -188,7 +200,7 @@ BI_GEMM_API int bi_rmsnorm_create(bi_rmsnorm_t* out, int64_t d, float eps) {
   const int nvec = int(d / birms::kVecElems);
   const int threads = birms::threads_for(d);
 
-  int dev = 0, major = 0, minor = 0, sms = 0, per_sm = 0;
+  int dev = 0, major = 0, minor = 0, sms = 0, per_sm = 0, per_sm_single = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -197,8 +209,10 @@ BI_GEMM_API int bi_rmsnorm_create(bi_rmsnorm_t* out, int64_t d, float eps) {
     return BI_GEMM_ERR_CUDA;
   }
   if (major != 10 || minor != 3) return BI_GEMM_ERR_UNSUPPORTED;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, birms::rmsnorm_kernel<false>, threads, 0) !=
-      cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, birms::rmsnorm_kernel<false, true>, threads, 0) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_single, birms::rmsnorm_kernel<false, false>, threads,
+                                                    0) != cudaSuccess) {
     cudaGetLastError();
     return BI_GEMM_ERR_CUDA;
   }
@@ -211,6 +225,7 @@ BI_GEMM_API int bi_rmsnorm_create(bi_rmsnorm_t* out, int64_t d, float eps) {
   h->vecs_per_thread = (nvec + threads - 1) / threads;
   h->num_sms = sms;
   h->max_ctas = std::max(1, per_sm) * sms;
+  h->max_ctas_single = std::max(1, per_sm_single) * sms;
   *out = h;
   return BI_GEMM_OK;
 }
@@ -238,7 +253,11 @@ BI_GEMM_API int bi_rmsnorm_run(bi_rmsnorm_t h, const void* x, int64_t M, const v
   p.eps = h->eps;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(unsigned(std::min<int64_t>(M, h->max_ctas)));
+  // Rows that outnumber the persistent build's resident blocks but not the single-row build's:
+  // every row its own block (the persistent build would give some blocks two rows in turn).
+  // Fewer rows run the persistent build, one row per block too, without its register cap.
+  const bool single = M > h->max_ctas && M <= h->max_ctas_single;
+  cfg.gridDim = dim3(unsigned(single ? M : std::min<int64_t>(M, h->max_ctas)));
   cfg.blockDim = dim3(unsigned(h->threads));
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
@@ -246,7 +265,8 @@ BI_GEMM_API int bi_rmsnorm_run(bi_rmsnorm_t h, const void* x, int64_t M, const v
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, birms::rmsnorm_kernel<false>, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, single ? birms::rmsnorm_kernel<false, false> : birms::rmsnorm_kernel<false, true>,
+                         p) != cudaSuccess) {
     cudaGetLastError();
     return BI_GEMM_ERR_CUDA;
   }

@@ -106,6 +106,11 @@ def test_large_batch_sampled_rows():
     check_rms(y[rows], v, "M=8192 sample")
     for r in rows[:16]:
         assert np.array_equal(host_bits(n(xd[r:r + 1].contiguous(), gd)), y[r:r + 1]), r
+    # batches just past the persistent grid's resident blocks (each row then has a block of its
+    # own, without the next-row prefetch): the same bits as in the batch of 8192
+    maxc = n.config["max_ctas"]
+    for M2 in (maxc + 1, 2000, 2 * maxc):
+        assert np.array_equal(host_bits(n(xd[:M2].contiguous(), gd)), y[:M2]), M2
     n.close()
 
 
