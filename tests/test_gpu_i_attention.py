@@ -203,6 +203,38 @@ def test_merge_of_long_split_lists():
     attn.close()
 
 
+def test_positions_written_by_the_preceding_kernel():
+    """The tokens' positions written on the stream by a kernel right before each call, as a serving
+    loop's scheduler does: each output equals that of the same call with the positions written
+    and the device synchronised first (the attention and merge kernels start before the kernel
+    before them has finished and must still read the new positions), for a small batch (unit
+    records derived in the attention kernel) and a larger one (the plan kernel first)."""
+    Hq, Hkv, D = 32, 8, 128
+    for lens in ([5000, 3000], [700] * 40):
+        bt = decode_batch(lens, Hq, Hkv, D, 16)
+        attn = BiAttention(Hq, Hkv, D, 16)
+        d = {k: torch.from_numpy(getattr(bt, k)).cuda() for k in ("q_seq", "q_pos", "table")}
+        bf = {k: torch.from_numpy(getattr(bt, k).view(np.int16)).cuda().view(torch.bfloat16)
+              for k in ("q", "kc", "vc")}
+        sets = [bt.q_pos, bt.q_pos // 2, np.maximum(bt.q_pos - 777, 0)]
+        srcs = [torch.from_numpy(ps.astype(np.int32)).cuda() for ps in sets]
+        refs = []
+        for src in srcs:
+            d["q_pos"].copy_(src)
+            torch.cuda.synchronize()
+            refs.append(attn.run(bf["q"], d["q_seq"], d["q_pos"], bf["kc"], bf["vc"], d["table"], bt.max_pos).clone())
+            torch.cuda.synchronize()
+        outs = []
+        for i in range(9):
+            torch.add(srcs[i % 3], 0, out=d["q_pos"])      # a kernel on the stream writes the positions
+            outs.append(attn.run(bf["q"], d["q_seq"], d["q_pos"], bf["kc"], bf["vc"], d["table"], bt.max_pos))
+        torch.cuda.synchronize()
+        assert attn.device_error() == 0
+        for i, o in enumerate(outs):
+            assert torch.equal(o.view(torch.int16), refs[i % 3].view(torch.int16)), (lens[:2], i)
+        attn.close()
+
+
 def test_repeat_runs_identical():
     bt = decode_batch([300, 5000, 17, 1024], 32, 8, 128, 16)
     attn = BiAttention(32, 8, 128, 16)
