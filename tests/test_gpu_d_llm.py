@@ -54,6 +54,30 @@ def test_rows_bitwise_identical_across_m(setup):
     assert g.device_error() == 0
 
 
+def test_static_w_with_x_written_just_before(setup):
+    """BI_GEMM_FLAG_STATIC_W: W is declared unwritten by running kernels, so each launch issues
+    its first W loads before the previous kernel in the stream has finished and only x waits for
+    that kernel.  Here a kernel writes x into the same buffer right before every launch, with
+    content alternating between two matrices, over the whole sweep back to back: every output
+    equals the same rows computed without the flag."""
+    g, W, X, Wd, Xd, y_full = setup
+    Bd = dev_bf16(ig.normal_bf16(ig.SEED_A, MMAX, K))
+    y_b = g(Bd, Wd)
+    gs = BiGemm(K, N, "bf16", static_w=True)
+    xbuf = torch.empty_like(Xd)
+    outs = []
+    for M in M_LIST:
+        for which, src in ((0, Xd), (1, Bd)):
+            torch.mul(src[:M], 1, out=xbuf[:M])        # exact; a kernel on the stream
+            outs.append((M, which, gs(xbuf[:M], Wd)))
+    torch.cuda.synchronize()
+    assert gs.device_error() == 0
+    for M, which, y in outs:
+        ref = (y_full, y_b)[which][:M]
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), (M, which)
+    gs.close()
+
+
 def test_parity_sampled_rows(setup):
     g, W, X, Wd, Xd, y_full = setup
     rows = sample_rows()

@@ -106,6 +106,34 @@ def test_mxfp8_llm_shape():
     g.close()
 
 
+def test_mxfp8_static_w_with_x_written_just_before():
+    """MXFP8 with BI_GEMM_FLAG_STATIC_W on the LLM shape: x and its scales written by kernels into
+    the same buffers right before every launch, alternating between two contents, back to back
+    at batch sizes on both sides of the pipeline switches: the bits of the same rows without the
+    flag."""
+    K, N, MM = 4096, 14336, 2048
+    xa, sxa, w, sw = inputs(K, N, ("VAR", "VAR"), rows=MM)
+    xb, sxb, _, _ = inputs(K, N, ("VAR", "VAR"), rows=MM, seed_x=ig.SEED_A)
+    g = BiGemm(K, N, "mxfp8")
+    gs = BiGemm(K, N, "mxfp8", static_w=True)
+    wd, swd = dev_u8(w), dev_u8(sw)
+    src = [(dev_u8(xa), dev_u8(sxa)), (dev_u8(xb), dev_u8(sxb))]
+    refs = [g(x, wd, sx=sx, sw=swd) for x, sx in src]
+    xbuf, sxbuf = torch.empty_like(src[0][0]), torch.empty_like(src[0][1])
+    outs = []
+    for M in (1, 17, 64, 65, 256, 1000, 2048):
+        for which in (0, 1):
+            torch.bitwise_or(src[which][0][:M], 0, out=xbuf[:M])     # kernels on the stream
+            torch.bitwise_or(src[which][1][:M], 0, out=sxbuf[:M])
+            outs.append((M, which, gs(xbuf[:M], wd, sx=sxbuf[:M], sw=swd)))
+    torch.cuda.synchronize()
+    assert gs.device_error() == 0
+    for M, which, y in outs:
+        assert torch.equal(y.view(torch.int16), refs[which][:M].view(torch.int16)), (M, which)
+    g.close()
+    gs.close()
+
+
 @pytest.mark.parametrize("K,N,M,split", [
     (512, 272, 300, 0),     # last pair tile: 16 columns in the leader's half, none in the peer's
     (1024, 400, 257, 0),    # last pair tile ends inside the peer's half; M one past a pair tile
