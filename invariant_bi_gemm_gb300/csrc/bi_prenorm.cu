@@ -87,6 +87,9 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(const Params p) {
   const int s = int(blockIdx.x);
   const int64_t row0 = int64_t(blockIdx.y) * kRows;
   const int32_t k0 = s * p.chunk;
+  // launched as a programmatic dependent: x may be the previous kernel's output and the
+  // workspace its input, so nothing global is touched before that kernel has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // stage the chunk: x rows (zeros past M or K) and W rows (zeros past K), 16-byte pieces
   const int xc = p.chunk / 8;   // pieces per x row
@@ -282,16 +285,28 @@ BI_GEMM_API int bi_prenorm_run(bi_prenorm_t h, const void* x, int64_t M, const v
   p.chunk = h->chunk;
   p.S = h->S;
   p.eps = h->eps;
-  biprn::chunk_kernel<<<dim3(unsigned(h->S), unsigned((M + biprn::kRows - 1) / biprn::kRows)), biprn::kThreads,
-                        h->smem, st>>>(p);
+  // Both kernels are programmatic dependents of the kernel before them: each launches while
+  // that kernel finishes and waits for it (griddepcontrol.wait) before touching global memory.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cc;
+  std::memset(&cc, 0, sizeof(cc));
+  cc.gridDim = dim3(unsigned(h->S), unsigned((M + biprn::kRows - 1) / biprn::kRows));
+  cc.blockDim = dim3(biprn::kThreads);
+  cc.dynamicSmemBytes = h->smem;
+  cc.stream = st;
+  cc.attrs = attr;
+  cc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cc, biprn::chunk_kernel, p) != cudaSuccess) {
+    cudaGetLastError();
+    return BI_GEMM_ERR_CUDA;
+  }
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(unsigned(M));
   cfg.blockDim = dim3(biprn::kMergeThreads);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, biprn::merge_kernel, p) != cudaSuccess) {
