@@ -59,6 +59,28 @@ def test_rows_identical_for_every_m():
     h.close()
 
 
+def test_x_written_by_the_preceding_kernel():
+    """Both kernels of a call start while the kernel before them finishes: x written by a kernel
+    into the same buffer right before every call, alternating two contents, back to back over the
+    page's batch boundaries, gives the bits of the same calls made after a synchronisation."""
+    K, N = 16384, 24
+    w = dev_bf16(ig.normal_bf16(ig.SEED_W, K, N, std=0.02))
+    srcs = [dev_bf16(ig.scaled_rows_bf16(sd, 256, K)) for sd in (ig.SEED_X, ig.SEED_A)]
+    h = BiPreNorm(K, N, EPS)
+    refs = [h(src, w).clone() for src in srcs]
+    torch.cuda.synchronize()
+    xbuf = torch.empty_like(srcs[0])
+    outs = []
+    for M in BOUNDARIES:
+        for which in (0, 1):
+            torch.mul(srcs[which][:M], 1, out=xbuf[:M])     # exact; a kernel on the stream
+            outs.append((M, which, h(xbuf[:M], w)))
+    torch.cuda.synchronize()
+    for M, which, y in outs:
+        assert torch.equal(y.view(torch.int32), refs[which][:M].view(torch.int32)), (M, which)
+    h.close()
+
+
 def test_bi_cells_at_the_pages_batch_boundaries():
     K, N = 16384, 24
     h = BiPreNorm(K, N, EPS)
