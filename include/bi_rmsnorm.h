@@ -44,8 +44,12 @@ typedef struct {
   int32_t threads;             /* threads per row (one thread block), multiple of 32, 128..1024 */
   int32_t vectors_per_thread;  /* 16-byte vectors (8 elements) per thread: thread t owns
                                   vectors t, t + threads, ... of the row                      */
-  int32_t max_ctas;            /* grid bound: resident blocks per SM x SMs (a block loops
-                                  over rows blockIdx.x, blockIdx.x + gridDim.x, ...)         */
+  int32_t max_ctas;            /* grid bound of the persistent launch: resident blocks per
+                                  SM x SMs (a block loops over rows blockIdx.x, blockIdx.x +
+                                  gridDim.x, ..., loading its next row while it reduces one).
+                                  A batch with more rows than this but no more than a launch
+                                  capped at half the registers keeps resident runs that launch
+                                  instead, one block per row; the arithmetic is the same.      */
   int32_t num_sms;
 } bi_rmsnorm_config;
 
