@@ -47,9 +47,10 @@ typedef struct {
   int32_t max_ctas;            /* grid bound of the persistent launch: resident blocks per
                                   SM x SMs (a block loops over rows blockIdx.x, blockIdx.x +
                                   gridDim.x, ..., loading its next row while it reduces one).
-                                  A batch with more rows than this but no more than a launch
-                                  capped at half the registers keeps resident runs that launch
-                                  instead, one block per row; the arithmetic is the same.      */
+                                  A batch with more rows than this, but few enough for every
+                                  row to get a resident block of its own when the registers
+                                  are capped at half, runs that capped launch instead, one
+                                  block per row; the arithmetic is the same.                   */
   int32_t num_sms;
 } bi_rmsnorm_config;
 
